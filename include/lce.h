@@ -1,0 +1,174 @@
+/*
+ * lce.h -- chunked linear cross-entropy on one GB300 GPU (sm_103a): C ABI.
+ *
+ * What is computed.  Hidden states X[N,H] times the LM-head weight W[V,H]
+ * (the nn.Linear weight layout), plus an optional bias b[V], give logits
+ * z[i,v] = sum_h X[i,h] W[v,h] + b[v].  Against labels y[N] the loss is
+ *
+ *     lse[i] = ln sum_v exp(z[i,v])
+ *     loss   = (1 / n_valid) * sum over rows with y[i] != ignore_index
+ *                                  of (lse[i] - z[i, y[i]])
+ *
+ * and the gradients, with s = grad_scale * grad_output / n_valid, are
+ *
+ *     G[i,v]  = s * (exp(z[i,v] - lse[i]) - [v == y[i]])   (0 for ignored rows)
+ *     grad_X  = G W,   grad_W = G^T X,   grad_b = sum_i G[i,:]
+ *
+ * This is torch's cross_entropy(X W^T + b, y, ignore_index) with a mean over
+ * valid rows, as the chunk-loss plugin of LlamaFactory PR #10762 uses it
+ * (analysis page, section 4 "Chunk Loss 구현": per-chunk cross_entropy with
+ * reduction="none" and ignore_index = IGNORE_INDEX = -100; grad_weight and
+ * grad_bias accumulated in FP32 and cast back to the weight dtype), and with
+ * the valid-token normalisation of the same page's section 3 (BaseTrainer).
+ *
+ * Rows are processed in chunks of at most `chunk_rows` rows ("maximum
+ * flattened token rows per logits/CE chunk", same page, section 1 and 2);
+ * the TRL page "1M 토큰 이상 학습", section "청킹", explains why rows split
+ * cleanly.  The N x V logits never exist in memory: only per-chunk pieces do.
+ *
+ * Conventions for every entry point
+ *  - Layouts: row-major, contiguous.  X [N,H], W [V,H], grad_X like X,
+ *    grad_W and grad_W_acc like W, lse [N], y int64 [N] (torch.long).
+ *    bf16 values are passed as their 16-bit patterns (lce_bf16).
+ *  - Device pointers: every tensor argument is a device pointer unless
+ *    stated otherwise, aligned to 16 bytes; `ws` is aligned to 256 bytes.
+ *  - Sizes: N >= 1, V >= 1, H >= 64 with H % 64 == 0, V <= 2^31 - 1,
+ *    N <= 2^31 - 1.  Other shapes return LCE_ERR_UNSUPPORTED.
+ *  - chunk_rows: rows per chunk; 0 lets the library choose; < 0 is
+ *    LCE_ERR_INVALID_ARG (the plugin rejects a non-positive chunk size).
+ *  - Ownership: the caller allocates and owns every buffer, including the
+ *    workspace `ws` of at least lce_workspace_size() bytes.  The library
+ *    never allocates or frees device memory.
+ *  - Streams: all work is enqueued on `stream` in order; no call
+ *    synchronises except lce_check_status().
+ *  - Errors found on the host (bad sizes, null or misaligned pointers, a
+ *    short workspace) are returned before anything is enqueued.  Errors
+ *    found on the device (a label outside [0,V) that is not ignore_index,
+ *    a pipeline wait that timed out) are recorded in a status word inside
+ *    `ws` and read back by lce_check_status(); outputs are then undefined.
+ *    No kernel traps.
+ *  - n_valid == 0 gives loss = 0 and all-zero gradients (the trainer's
+ *    guard against dividing by zero); lse is still written for every row,
+ *    ignored rows included.
+ *  - Results of lse and loss do not depend on chunk_rows (bit for bit);
+ *    gradients depend on it only through the FP32 accumulation order.
+ */
+#ifndef LCE_H_
+#define LCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LCE_API __attribute__((visibility("default")))
+#else
+#define LCE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t lce_bf16;
+
+/* A CUDA stream (cudaStream_t and CUstream convert to it implicitly). */
+struct CUstream_st;
+typedef struct CUstream_st* lce_stream_t;
+
+typedef enum {
+    LCE_OK = 0,
+    LCE_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, negative size or chunk_rows */
+    LCE_ERR_UNSUPPORTED = 2,   /* shape outside the supported range (see above) */
+    LCE_ERR_WORKSPACE = 3,     /* ws_bytes smaller than lce_workspace_size() */
+    LCE_ERR_LABEL_RANGE = 4,   /* device: a label outside [0,V) and != ignore_index */
+    LCE_ERR_TIMEOUT = 5,       /* device: a pipeline wait exceeded its time limit */
+    LCE_ERR_CUDA = 6           /* a CUDA runtime call or launch failed */
+} lce_status_t;
+
+/* Which entry point a workspace is sized for. */
+enum { LCE_WS_FORWARD = 0, LCE_WS_BACKWARD = 1, LCE_WS_FUSED = 2 };
+
+/* Bytes of workspace the entry point `which` needs for this problem.
+ * Host only; enqueues nothing.  Writes *bytes on LCE_OK. */
+LCE_API lce_status_t lce_workspace_size(int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
+                                int has_bias, int which, size_t* bytes);
+
+/* Rows per chunk the library uses for (N, H, V, chunk_rows).  Host only. */
+LCE_API lce_status_t lce_chunk_rows(int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
+                            int64_t* rows_per_chunk);
+
+/* Forward: loss [1] (float), lse [N] (float) and n_valid [1] (int64).
+ * b may be NULL (no bias); n_valid may be NULL.
+ * Cost: 2*N*H*V tensor-core FLOPs. */
+LCE_API lce_status_t lce_forward(int64_t N, int64_t H, int64_t V,
+                         const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
+                         const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
+                         float* loss, float* lse, int64_t* n_valid,
+                         void* ws, size_t ws_bytes, lce_stream_t stream);
+
+/* Backward from a forward's lse [N]: the logits are recomputed per chunk.
+ * The gradient scale is grad_scale (host) times *d_grad_output (a device
+ * float; NULL means 1), divided by n_valid.
+ * grad_W_acc [V,H] float is required: it receives the FP32 accumulation
+ * (overwritten, not added to).  grad_W [V,H] bf16 receives its
+ * round-to-nearest-even cast and may be NULL.  grad_X [N,H] bf16 may be
+ * NULL (then the grad_X product is skipped).  With a bias, grad_b_acc [V]
+ * float and grad_b [V] bf16 follow the same rules (grad_b_acc required,
+ * grad_b optional); without a bias both must be NULL.
+ * Cost: 6*N*H*V tensor-core FLOPs (4 without grad_X). */
+LCE_API lce_status_t lce_backward(int64_t N, int64_t H, int64_t V,
+                          const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
+                          const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
+                          const float* lse, float grad_scale, const float* d_grad_output,
+                          lce_bf16* grad_X, lce_bf16* grad_W, lce_bf16* grad_b,
+                          float* grad_W_acc, float* grad_b_acc,
+                          void* ws, size_t ws_bytes, lce_stream_t stream);
+
+/* Forward and backward in one call (the saved-gradient design of the
+ * chunk-loss plugin): loss, lse, n_valid, and all gradients, with the same
+ * rules as lce_forward and lce_backward.  Cost: 8*N*H*V tensor-core FLOPs
+ * (forward logits, recomputed logits, grad_X, grad_W). */
+LCE_API lce_status_t lce_fused_fwd_bwd(int64_t N, int64_t H, int64_t V,
+                               const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
+                               const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
+                               float grad_scale, const float* d_grad_output,
+                               float* loss, float* lse, int64_t* n_valid,
+                               lce_bf16* grad_X, lce_bf16* grad_W, lce_bf16* grad_b,
+                               float* grad_W_acc, float* grad_b_acc,
+                               void* ws, size_t ws_bytes, lce_stream_t stream);
+
+/* Synchronises `stream`, then returns the device status of the last call
+ * that used workspace `ws` (LCE_OK, LCE_ERR_LABEL_RANGE, LCE_ERR_TIMEOUT),
+ * or LCE_ERR_CUDA if the stream reported an error. */
+LCE_API lce_status_t lce_check_status(const void* ws, lce_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+LCE_API const char* lce_status_string(lce_status_t status);
+
+/* ---- diagnostics (used by the tests; not part of the loss) -------------
+ *
+ * lce_debug_gemm: the library's tensor-core GEMM core alone, FP32 output
+ * D [M,N] (row-major) from bf16 operands, for the three operand layouts
+ * the loss uses:
+ *   layout 0: A [M,K], B [N,K]   D = A B^T   (logits:  X_c W^T)
+ *   layout 1: A [M,K], B [K,N]   D = A B     (grad_X:  G W)
+ *   layout 2: A [K,M], B [K,N]   D = A^T B   (grad_W:  G^T X_c)
+ * M, N, K >= 1 and multiples of 8.  ws >= 256 bytes holds the status word.
+ *
+ * lce_debug_wait_timeout: one block waits on a pipeline barrier that is
+ * never signalled, through the same bounded wait as the GEMM pipeline,
+ * with a limit of `limit_us` microseconds; the status word in `ws`
+ * (>= 256 bytes) then reads LCE_ERR_TIMEOUT.  Shows that a stuck pipeline
+ * ends with an error status instead of a hang. */
+LCE_API lce_status_t lce_debug_gemm(int layout, int64_t M, int64_t N, int64_t K,
+                            const lce_bf16* A, const lce_bf16* B, float* D,
+                            void* ws, size_t ws_bytes, lce_stream_t stream);
+
+LCE_API lce_status_t lce_debug_wait_timeout(uint32_t limit_us, void* ws, size_t ws_bytes,
+                                    lce_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LCE_H_ */

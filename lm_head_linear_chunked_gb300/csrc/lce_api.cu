@@ -1,0 +1,479 @@
+// Host side of the library: argument checks, the chunk planner, workspace
+// carving, TMA descriptor encoding, and the launch sequence of each entry
+// point of lce.h.
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "lce_internal.cuh"
+
+namespace lce {
+namespace {
+
+constexpr int64_t AUTO_CHUNK_ROWS = 8192;
+constexpr size_t HEADER_BYTES = 1024;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Plan {
+    int64_t N, H, V, C, n_chunks, n_vt, ldg, mt_chunk, label_blocks_per_chunk;
+    bool has_bias;
+    size_t off_row_loss, off_zt, off_pm, off_ps, off_g, off_gb, off_keys, off_counts, off_w16, off_x16, total;
+};
+
+lce_status_t check_sizes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows) {
+    if (N <= 0 || H <= 0 || V <= 0 || chunk_rows < 0) return LCE_ERR_INVALID_ARG;
+    if (H % 64 != 0 || N > INT32_MAX || V > INT32_MAX || H > INT32_MAX) return LCE_ERR_UNSUPPORTED;
+    return LCE_OK;
+}
+
+int64_t rows_per_chunk(int64_t N, int64_t chunk_rows) {
+    const int64_t c = chunk_rows > 0 ? chunk_rows : AUTO_CHUNK_ROWS;
+    return c < N ? c : N;
+}
+
+lce_status_t make_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, bool has_bias, int which,
+                       Plan* p) {
+    lce_status_t st = check_sizes(N, H, V, chunk_rows);
+    if (st != LCE_OK) return st;
+    if (which < LCE_WS_FORWARD || which > LCE_WS_FUSED) return LCE_ERR_INVALID_ARG;
+    p->N = N;
+    p->H = H;
+    p->V = V;
+    p->C = rows_per_chunk(N, chunk_rows);
+    p->n_chunks = cdiv(N, p->C);
+    p->n_vt = cdiv(V, BN);
+    p->ldg = align_up(static_cast<size_t>(V), 8);
+    p->mt_chunk = cdiv(p->C, BM);
+    p->label_blocks_per_chunk = cdiv(p->C, LABEL_BLOCK);
+    p->has_bias = has_bias;
+    const bool fwd = which != LCE_WS_BACKWARD, bwd = which != LCE_WS_FORWARD;
+    size_t off = HEADER_BYTES;
+    auto take = [&](bool use, size_t bytes) -> size_t {
+        if (!use) return 0;
+        const size_t at = off;
+        off = align_up(off + bytes, 1024);
+        return at;
+    };
+    p->off_row_loss = take(fwd, static_cast<size_t>(N) * 4);
+    p->off_zt = take(fwd, static_cast<size_t>(p->C) * 4);
+    p->off_pm = take(fwd, static_cast<size_t>(p->n_vt) * p->C * 4);
+    p->off_ps = take(fwd, static_cast<size_t>(p->n_vt) * p->C * 4);
+    p->off_g = take(bwd, static_cast<size_t>(p->C) * p->ldg * 2);
+    p->off_gb = take(bwd && has_bias, static_cast<size_t>(p->mt_chunk) * 4 * V * 4);
+    p->off_keys = take(bwd, static_cast<size_t>(p->n_chunks) * p->label_blocks_per_chunk * LABEL_BLOCK * 8);
+    p->off_counts = take(bwd && has_bias, static_cast<size_t>(V) * 4);
+    p->off_w16 = take(bwd, static_cast<size_t>(V) * H * 2);
+    p->off_x16 = take(bwd, static_cast<size_t>(p->C) * H * 2);
+    p->total = off;
+    return LCE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- TMA maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Row-major 16-bit matrix [rows, cols] (bf16, or fp16 with `fp16`) with row
+// pitch `pitch` elements; boxes of box_cols (innermost, 64 = one 128-byte
+// swizzle row) x box_rows.  Out-of-range elements of a box read as zero.
+bool map_16bit_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t pitch,
+                  uint32_t box_cols, uint32_t box_rows, bool fp16 = false) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch) * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= 64) return 0;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+int grid_for(int64_t tiles) {
+    const int sms = sm_count();
+    if (sms <= 0) return 0;
+    return static_cast<int>(tiles < sms ? tiles : sms);
+}
+
+GemmArgs base_args(WsHeader* hdr) {
+    GemmArgs a;
+    memset(&a, 0, sizeof(a));
+    a.group_m = 1;
+    a.status = &hdr->status;
+    a.timeout_ns = WAIT_LIMIT_NS;
+    return a;
+}
+
+#define LCE_TRY_CUDA(expr)                          \
+    do {                                            \
+        if ((expr) != cudaSuccess) return LCE_ERR_CUDA; \
+    } while (0)
+
+// ---------------------------------------------------------------- the loss
+
+struct Problem {
+    int64_t N, H, V;
+    const uint16_t *X, *W, *b;
+    const int64_t* y;
+    int64_t ignore_index;
+};
+
+struct Outputs {
+    float* loss;
+    float* lse;  // written by the forward; read by the backward
+    int64_t* n_valid;
+    float grad_scale;
+    const float* d_grad_output;
+    uint16_t *grad_X, *grad_W, *grad_b;
+    float *grad_W_acc, *grad_b_acc;
+};
+
+lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, int64_t chunk_rows, void* ws,
+                 size_t ws_bytes, cudaStream_t s) {
+    Plan p;
+    const int which = do_fwd && do_bwd ? LCE_WS_FUSED : (do_fwd ? LCE_WS_FORWARD : LCE_WS_BACKWARD);
+    lce_status_t st = make_plan(pb.N, pb.H, pb.V, chunk_rows, pb.b != nullptr, which, &p);
+    if (st != LCE_OK) return st;
+    // pointer checks
+    if (!pb.X || !pb.W || !pb.y || !ws || !o.lse) return LCE_ERR_INVALID_ARG;
+    if (!aligned16(pb.X) || !aligned16(pb.W) || !aligned16(pb.b) || !aligned16(pb.y) || !aligned16(o.lse) ||
+        (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+        return LCE_ERR_INVALID_ARG;
+    if (do_fwd && !o.loss) return LCE_ERR_INVALID_ARG;
+    if (do_bwd) {
+        if (!o.grad_W_acc || !aligned16(o.grad_W_acc) || !aligned16(o.grad_W) || !aligned16(o.grad_X))
+            return LCE_ERR_INVALID_ARG;
+        if (pb.b) {
+            if (!o.grad_b_acc) return LCE_ERR_INVALID_ARG;
+        } else if (o.grad_b || o.grad_b_acc) {
+            return LCE_ERR_INVALID_ARG;
+        }
+    }
+    if (ws_bytes < p.total) return LCE_ERR_WORKSPACE;
+    if (!encode_fn() || sm_count() <= 0) return LCE_ERR_CUDA;
+
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(wsb);
+    float* row_loss = do_fwd ? reinterpret_cast<float*>(wsb + p.off_row_loss) : nullptr;
+    float* zt = do_fwd ? reinterpret_cast<float*>(wsb + p.off_zt) : nullptr;
+    float* pm = do_fwd ? reinterpret_cast<float*>(wsb + p.off_pm) : nullptr;
+    float* ps = do_fwd ? reinterpret_cast<float*>(wsb + p.off_ps) : nullptr;
+    uint16_t* G = do_bwd ? reinterpret_cast<uint16_t*>(wsb + p.off_g) : nullptr;
+    float* gb = (do_bwd && pb.b) ? reinterpret_cast<float*>(wsb + p.off_gb) : nullptr;
+    unsigned long long* keys = do_bwd ? reinterpret_cast<unsigned long long*>(wsb + p.off_keys) : nullptr;
+    uint16_t* W16 = do_bwd ? reinterpret_cast<uint16_t*>(wsb + p.off_w16) : nullptr;
+    uint16_t* X16 = do_bwd ? reinterpret_cast<uint16_t*>(wsb + p.off_x16) : nullptr;
+    int* counts = (do_bwd && pb.b) ? reinterpret_cast<int*>(wsb + p.off_counts) : nullptr;
+
+    // operand maps of the whole X and W
+    CUtensorMap mX_k, mW_k, mW16_mn;
+    if (!map_16bit_2d(&mX_k, pb.X, pb.N, pb.H, pb.H, 64, BM) || !map_16bit_2d(&mW_k, pb.W, pb.V, pb.H, pb.H, 64, BN))
+        return LCE_ERR_CUDA;
+    if (do_bwd && !map_16bit_2d(&mW16_mn, W16, pb.V, pb.H, pb.H, 64, 64, true)) return LCE_ERR_CUDA;
+
+    LCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
+    if (counts) LCE_TRY_CUDA(cudaMemsetAsync(counts, 0, static_cast<size_t>(pb.V) * 4, s));
+    LCE_TRY_CUDA(launch_prepass(pb.y, pb.N, pb.V, pb.ignore_index, hdr, counts, s));
+    if (do_bwd) {
+        LCE_TRY_CUDA(launch_scale(hdr, o.grad_scale, o.d_grad_output, nullptr, s));
+        LCE_TRY_CUDA(launch_label_sort(pb.y, pb.N, p.C, p.label_blocks_per_chunk,
+                                       p.n_chunks * p.label_blocks_per_chunk, pb.V, pb.ignore_index, keys, s));
+        // fp16 operands of the gradient GEMMs, with exact power-of-two scales
+        LCE_TRY_CUDA(launch_amax(pb.X, pb.N * pb.H, &hdr->amax_x_bits, s));
+        LCE_TRY_CUDA(launch_amax(pb.W, pb.V * pb.H, &hdr->amax_w_bits, s));
+        LCE_TRY_CUDA(launch_to_f16_scaled(pb.W, pb.V * pb.H, &hdr->amax_w_bits, W16, s));
+    }
+
+    for (int64_t c = 0; c < p.n_chunks; ++c) {
+        const int64_t r0 = c * p.C;
+        const int64_t rows = (pb.N - r0) < p.C ? (pb.N - r0) : p.C;
+        const int64_t mt = cdiv(rows, BM);
+        if (do_fwd) {
+            GemmArgs a = base_args(hdr);
+            a.m_tiles = static_cast<int32_t>(mt);
+            a.n_tiles = static_cast<int32_t>(p.n_vt);
+            a.k_blocks = static_cast<int32_t>(cdiv(pb.H, BK));
+            a.raster = 0;
+            a.a_y0 = static_cast<int32_t>(r0);
+            a.M = rows;
+            a.N = pb.V;
+            a.y = pb.y + r0;
+            a.ignore_index = pb.ignore_index;
+            a.bias = pb.b;
+            a.part_m = pm;
+            a.part_s = ps;
+            a.zt = zt;
+            a.ldp = p.C;
+            LCE_TRY_CUDA(launch_gemm(MODE_LSE, mX_k, mW_k, a, grid_for(mt * p.n_vt), s));
+            LCE_TRY_CUDA(launch_combine(pm, ps, p.n_vt, p.C, rows, zt, pb.y + r0, pb.ignore_index, o.lse + r0,
+                                        row_loss + r0, s));
+        }
+        if (do_bwd) {
+            const bool first = c == 0, last = c == p.n_chunks - 1;
+            {   // recompute the logits; P = softmax (bf16)
+                GemmArgs a = base_args(hdr);
+                a.m_tiles = static_cast<int32_t>(mt);
+                a.n_tiles = static_cast<int32_t>(p.n_vt);
+                a.k_blocks = static_cast<int32_t>(cdiv(pb.H, BK));
+                a.raster = 0;
+                a.a_y0 = static_cast<int32_t>(r0);
+                a.M = rows;
+                a.N = pb.V;
+                a.y = pb.y + r0;
+                a.ignore_index = pb.ignore_index;
+                a.bias = pb.b;
+                a.lse = o.lse + r0;
+                a.g = G;
+                a.ldg = p.ldg;
+                a.gb_part = gb;
+                LCE_TRY_CUDA(launch_gemm(MODE_G, mX_k, mW_k, a, grid_for(mt * p.n_vt), s));
+            }
+            if (gb)
+                LCE_TRY_CUDA(launch_grad_b(gb, mt * 4, pb.V, hdr, counts, o.grad_b_acc, o.grad_b, first, last, s));
+            // P and X_c maps bounded to this chunk's rows: rows past it read as zero
+            LCE_TRY_CUDA(launch_to_f16_scaled(pb.X + r0 * pb.H, rows * pb.H, &hdr->amax_x_bits, X16, s));
+            CUtensorMap mG_k, mG_mn, mX16_mn;
+            if (!map_16bit_2d(&mG_k, G, rows, pb.V, p.ldg, 64, BM, true) ||
+                !map_16bit_2d(&mG_mn, G, rows, pb.V, p.ldg, 64, 64, true) ||
+                !map_16bit_2d(&mX16_mn, X16, rows, pb.H, pb.H, 64, 64, true))
+                return LCE_ERR_CUDA;
+            if (o.grad_X) {   // grad_X_c = s (P W - W[y])
+                GemmArgs a = base_args(hdr);
+                a.m_tiles = static_cast<int32_t>(mt);
+                a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
+                a.k_blocks = static_cast<int32_t>(cdiv(pb.V, BK));
+                a.raster = 2;
+                a.group_m = 16;
+                a.M = rows;
+                a.N = pb.H;
+                a.scale = &hdr->scale;
+                a.out_bf16 = o.grad_X + r0 * pb.H;
+                a.ld_out = pb.H;
+                a.y = pb.y + r0;
+                a.ignore_index = pb.ignore_index;
+                a.w_rows = pb.W;
+                a.ldw = pb.H;
+                a.V = pb.V;
+                a.b_amax_bits = &hdr->amax_w_bits;
+                LCE_TRY_CUDA(launch_gemm(MODE_GRADX, mG_k, mW16_mn, a, grid_for(static_cast<int64_t>(a.m_tiles) * a.n_tiles), s));
+            }
+            {   // grad_W_acc (+)= s P^T X_c
+                GemmArgs a = base_args(hdr);
+                a.m_tiles = static_cast<int32_t>(cdiv(pb.V, BM));
+                a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
+                a.k_blocks = static_cast<int32_t>(cdiv(rows, BK));
+                a.raster = 1;
+                a.M = pb.V;
+                a.N = pb.H;
+                a.scale = &hdr->scale;
+                a.out_f32 = o.grad_W_acc;
+                a.ld_f32 = pb.H;
+                a.out_bf16 = o.grad_W;
+                a.ld_out = pb.H;
+                a.acc_first = first;
+                a.write_bf16 = last && o.grad_W != nullptr;
+                a.b_amax_bits = &hdr->amax_x_bits;
+                LCE_TRY_CUDA(launch_gemm(MODE_GRADW, mG_mn, mX16_mn, a, grid_for(static_cast<int64_t>(a.m_tiles) * a.n_tiles), s));
+            }
+            // grad_W_acc[y_i] -= s X[i] for the chunk's valid rows, exactly, in row order
+            for (int64_t k = 0; k < p.label_blocks_per_chunk; ++k) {
+                const int64_t n = rows - k * LABEL_BLOCK;
+                if (n <= 0) break;
+                LCE_TRY_CUDA(launch_onehot_scatter(keys + (c * p.label_blocks_per_chunk + k) * LABEL_BLOCK,
+                                                   n < LABEL_BLOCK ? n : LABEL_BLOCK, pb.X + r0 * pb.H, pb.H, hdr,
+                                                   o.grad_W_acc, o.grad_W, last && o.grad_W != nullptr, s));
+            }
+        }
+    }
+    if (do_fwd) LCE_TRY_CUDA(launch_loss(row_loss, pb.N, hdr, o.loss, o.n_valid, s));
+    return LCE_OK;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
+                        int grid, cudaStream_t stream) {
+    if (grid <= 0) return cudaErrorInvalidConfiguration;
+    switch (mode) {
+        case MODE_LSE:
+        case MODE_G: return launch_gemm_logits(mode, map_a, map_b, args, grid, stream);
+        case MODE_GRADX:
+        case MODE_GRADW: return launch_gemm_grads(mode, map_a, map_b, args, grid, stream);
+        default: return launch_gemm_plain(mode, map_a, map_b, args, grid, stream);
+    }
+}
+
+}  // namespace lce
+
+using namespace lce;
+
+extern "C" {
+
+lce_status_t lce_workspace_size(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, int has_bias, int which,
+                                size_t* bytes) {
+    if (!bytes) return LCE_ERR_INVALID_ARG;
+    Plan p;
+    const lce_status_t st = make_plan(N, H, V, chunk_rows, has_bias != 0, which, &p);
+    if (st == LCE_OK) *bytes = p.total;
+    return st;
+}
+
+lce_status_t lce_chunk_rows(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, int64_t* out) {
+    if (!out) return LCE_ERR_INVALID_ARG;
+    const lce_status_t st = check_sizes(N, H, V, chunk_rows);
+    if (st == LCE_OK) *out = rows_per_chunk(N, chunk_rows);
+    return st;
+}
+
+lce_status_t lce_forward(int64_t N, int64_t H, int64_t V, const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
+                         const int64_t* y, int64_t ignore_index, int64_t chunk_rows, float* loss, float* lse,
+                         int64_t* n_valid, void* ws, size_t ws_bytes, lce_stream_t stream) {
+    Problem pb{N, H, V, X, W, b, y, ignore_index};
+    Outputs o;
+    memset(&o, 0, sizeof(o));
+    o.loss = loss;
+    o.lse = lse;
+    o.n_valid = n_valid;
+    return run(pb, o, true, false, chunk_rows, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lce_status_t lce_backward(int64_t N, int64_t H, int64_t V, const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
+                          const int64_t* y, int64_t ignore_index, int64_t chunk_rows, const float* lse,
+                          float grad_scale, const float* d_grad_output, lce_bf16* grad_X, lce_bf16* grad_W,
+                          lce_bf16* grad_b, float* grad_W_acc, float* grad_b_acc, void* ws, size_t ws_bytes,
+                          lce_stream_t stream) {
+    Problem pb{N, H, V, X, W, b, y, ignore_index};
+    Outputs o;
+    memset(&o, 0, sizeof(o));
+    o.lse = const_cast<float*>(lse);
+    o.grad_scale = grad_scale;
+    o.d_grad_output = d_grad_output;
+    o.grad_X = grad_X;
+    o.grad_W = grad_W;
+    o.grad_b = grad_b;
+    o.grad_W_acc = grad_W_acc;
+    o.grad_b_acc = grad_b_acc;
+    return run(pb, o, false, true, chunk_rows, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lce_status_t lce_fused_fwd_bwd(int64_t N, int64_t H, int64_t V, const lce_bf16* X, const lce_bf16* W,
+                               const lce_bf16* b, const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
+                               float grad_scale, const float* d_grad_output, float* loss, float* lse,
+                               int64_t* n_valid, lce_bf16* grad_X, lce_bf16* grad_W, lce_bf16* grad_b,
+                               float* grad_W_acc, float* grad_b_acc, void* ws, size_t ws_bytes,
+                               lce_stream_t stream) {
+    Problem pb{N, H, V, X, W, b, y, ignore_index};
+    Outputs o;
+    memset(&o, 0, sizeof(o));
+    o.loss = loss;
+    o.lse = lse;
+    o.n_valid = n_valid;
+    o.grad_scale = grad_scale;
+    o.d_grad_output = d_grad_output;
+    o.grad_X = grad_X;
+    o.grad_W = grad_W;
+    o.grad_b = grad_b;
+    o.grad_W_acc = grad_W_acc;
+    o.grad_b_acc = grad_b_acc;
+    return run(pb, o, true, true, chunk_rows, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lce_status_t lce_check_status(const void* ws, lce_stream_t stream) {
+    if (!ws) return LCE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LCE_ERR_CUDA;
+    unsigned st = 0;
+    if (cudaMemcpy(&st, ws, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return LCE_ERR_CUDA;
+    if (st & STATUS_TIMEOUT) return LCE_ERR_TIMEOUT;
+    if (st & STATUS_LABEL) return LCE_ERR_LABEL_RANGE;
+    return LCE_OK;
+}
+
+const char* lce_status_string(lce_status_t status) {
+    switch (status) {
+        case LCE_OK: return "ok";
+        case LCE_ERR_INVALID_ARG: return "invalid argument";
+        case LCE_ERR_UNSUPPORTED: return "unsupported shape";
+        case LCE_ERR_WORKSPACE: return "workspace too small";
+        case LCE_ERR_LABEL_RANGE: return "label out of range";
+        case LCE_ERR_TIMEOUT: return "device wait timed out";
+        case LCE_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+lce_status_t lce_debug_gemm(int layout, int64_t M, int64_t N, int64_t K, const lce_bf16* A, const lce_bf16* B,
+                            float* D, void* ws, size_t ws_bytes, lce_stream_t stream) {
+    if (layout < 0 || layout > 2 || M <= 0 || N <= 0 || K <= 0 || !A || !B || !D || !ws) return LCE_ERR_INVALID_ARG;
+    if (M % 8 || N % 8 || K % 8 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return LCE_ERR_UNSUPPORTED;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return LCE_ERR_INVALID_ARG;
+    if (ws_bytes < 256) return LCE_ERR_WORKSPACE;
+    if (!encode_fn() || sm_count() <= 0) return LCE_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    WsHeader* hdr = static_cast<WsHeader*>(ws);
+    CUtensorMap ma, mb;
+    bool ok;
+    if (layout == 0)
+        ok = map_16bit_2d(&ma, A, M, K, K, 64, BM) && map_16bit_2d(&mb, B, N, K, K, 64, BN);
+    else if (layout == 1)
+        ok = map_16bit_2d(&ma, A, M, K, K, 64, BM) && map_16bit_2d(&mb, B, K, N, N, 64, 64);
+    else
+        ok = map_16bit_2d(&ma, A, K, M, M, 64, 64) && map_16bit_2d(&mb, B, K, N, N, 64, 64);
+    if (!ok) return LCE_ERR_CUDA;
+    GemmArgs a = base_args(hdr);
+    a.m_tiles = static_cast<int32_t>(cdiv(M, BM));
+    a.n_tiles = static_cast<int32_t>(cdiv(N, BN));
+    a.k_blocks = static_cast<int32_t>(cdiv(K, BK));
+    a.raster = 0;
+    a.M = M;
+    a.N = N;
+    a.out_f32 = D;
+    a.ld_f32 = N;
+    LCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
+    LCE_TRY_CUDA(launch_gemm(layout, ma, mb, a, grid_for(static_cast<int64_t>(a.m_tiles) * a.n_tiles), s));
+    return LCE_OK;
+}
+
+lce_status_t lce_debug_wait_timeout(uint32_t limit_us, void* ws, size_t ws_bytes, lce_stream_t stream) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return LCE_ERR_INVALID_ARG;
+    if (ws_bytes < 256) return LCE_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    WsHeader* hdr = static_cast<WsHeader*>(ws);
+    LCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
+    LCE_TRY_CUDA(launch_wait_probe(&hdr->status, static_cast<uint64_t>(limit_us) * 1000ull, s));
+    return LCE_OK;
+}
+
+}  // extern "C"

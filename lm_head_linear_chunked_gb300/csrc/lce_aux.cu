@@ -1,0 +1,378 @@
+// The loss's small kernels: label check and valid-row count, gradient scale,
+// per-row logsumexp combine, the fixed-order loss reduction, the label sort
+// and exact one-hot part of grad_W, the grad_b accumulation, and the
+// bounded-wait probe.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "lce_internal.cuh"
+#include "lce_ptx.cuh"
+
+namespace lce {
+
+namespace {
+
+constexpr float LN2_F = 0.6931471805599453f;
+
+// Labels must lie in [0, V) or equal ignore_index (cross_entropy's contract).
+// Counts the valid rows; a bad label raises the status bit and is not counted.
+// With `label_counts`, also counts each label's valid rows (integer
+// atomics: the result does not depend on their order).
+__global__ void prepass_kernel(const int64_t* __restrict__ y, int64_t N, int64_t V,
+                               int64_t ignore_index, WsHeader* hdr, int* label_counts) {
+    unsigned long long cnt = 0;
+    bool bad = false;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < N;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t v = y[i];
+        if (v == ignore_index) continue;
+        if (v < 0 || v >= V) {
+            bad = true;
+        } else {
+            ++cnt;
+            if (label_counts) atomicAdd(label_counts + v, 1);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+    __shared__ unsigned long long part[32];
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) part[w] = cnt;
+    if (__any_sync(0xFFFFFFFFu, bad) && l == 0) atomicOr(&hdr->status, STATUS_LABEL);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long s = 0;
+        for (int k = 0; k < (blockDim.x + 31) / 32; ++k) s += part[k];
+        atomicAdd(&hdr->n_valid, s);
+    }
+}
+
+// s = grad_scale * grad_output / n_valid (0 without valid rows).
+__global__ void scale_kernel(WsHeader* hdr, float grad_scale, const float* d_grad_output,
+                             int64_t* n_valid_out) {
+    const unsigned long long nv = hdr->n_valid;
+    const double go = d_grad_output ? static_cast<double>(*d_grad_output) : 1.0;
+    hdr->scale = nv ? static_cast<float>(static_cast<double>(grad_scale) * go / static_cast<double>(nv)) : 0.f;
+    if (n_valid_out) *n_valid_out = static_cast<int64_t>(nv);
+}
+
+// lse_i = (M + log2 sum_t s_t 2^(m_t - M)) ln 2 over the vocabulary tiles t,
+// in tile order; row loss = lse_i - z[i, y_i] for valid rows, else 0.
+__global__ void combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps, int64_t n_vt,
+                               int64_t ldp, int64_t rows, const float* __restrict__ zt,
+                               const int64_t* __restrict__ y, int64_t ignore_index,
+                               float* __restrict__ lse, float* __restrict__ row_loss) {
+    const int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (r >= rows) return;
+    float M = -INFINITY;
+    for (int64_t t = 0; t < n_vt; ++t) M = fmaxf(M, pm[t * ldp + r]);
+    float S = 0.f;
+    for (int64_t t = 0; t < n_vt; ++t) S += ps[t * ldp + r] * exp2f(pm[t * ldp + r] - M);
+    const float l = (M + log2f(S)) * LN2_F;
+    lse[r] = l;
+    if (row_loss) row_loss[r] = (y[r] != ignore_index) ? l - zt[r] : 0.f;
+}
+
+// loss = sum of row losses / n_valid.  One block; the summation order
+// depends on N only, so the result does not depend on the chunk size.
+__global__ void loss_kernel(const float* __restrict__ row_loss, int64_t N, const WsHeader* hdr,
+                            float* loss, int64_t* n_valid_out) {
+    __shared__ double red[1024];
+    double acc = 0.0;
+    for (int64_t i = threadIdx.x; i < N; i += blockDim.x) acc += static_cast<double>(row_loss[i]);
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+        if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const unsigned long long nv = hdr->n_valid;
+        *loss = nv ? static_cast<float>(red[0] / static_cast<double>(nv)) : 0.f;
+        if (n_valid_out) *n_valid_out = static_cast<int64_t>(nv);
+    }
+}
+
+// grad_b_acc (+)= s * sum over the chunk's partial column sums of P (fixed
+// order); on the last chunk the one-hot part, -s * (count of label v), is
+// subtracted exactly and grad_b = bf16(grad_b_acc).
+__global__ void grad_b_kernel(const float* __restrict__ gb_part, int64_t parts, int64_t V,
+                              const WsHeader* hdr, const int* __restrict__ label_counts, float* grad_b_acc,
+                              uint16_t* grad_b, int first, int last) {
+    const int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (v >= V) return;
+    float t = 0.f;
+    for (int64_t p = 0; p < parts; ++p) t += gb_part[p * V + v];
+    const float s = hdr->scale;
+    float a = first ? s * t : fmaf(s, t, grad_b_acc[v]);
+    if (last) a = fmaf(-s, static_cast<float>(label_counts[v]), a);
+    grad_b_acc[v] = a;
+    if (last && grad_b) {
+        __nv_bfloat16 h = __float2bfloat16_rn(a);
+        grad_b[v] = *reinterpret_cast<uint16_t*>(&h);
+    }
+}
+
+// Sorts one block of up to LABEL_BLOCK rows of a chunk by (label, row) with
+// a bitonic network in shared memory.  Ignored rows and out-of-range labels
+// get the largest key and end up last.  Key = label << 32 | row-in-chunk,
+// so rows of one label stay in row order.
+__global__ void __launch_bounds__(1024) label_sort_kernel(const int64_t* __restrict__ y, int64_t N, int64_t C,
+                                                          int64_t blocks_per_chunk, int64_t V,
+                                                          int64_t ignore_index,
+                                                          unsigned long long* __restrict__ keys_out) {
+    extern __shared__ unsigned long long sk[];
+    const int64_t b = blockIdx.x;
+    const int64_t chunk_start = (b / blocks_per_chunk) * C;
+    const int64_t chunk_end = chunk_start + C < N ? chunk_start + C : N;
+    const int64_t start = chunk_start + (b % blocks_per_chunk) * LABEL_BLOCK;
+    const int64_t left = chunk_end - start;
+    const int count = left <= 0 ? 0 : (left < LABEL_BLOCK ? static_cast<int>(left) : LABEL_BLOCK);
+    for (int i = threadIdx.x; i < LABEL_BLOCK; i += blockDim.x) {
+        unsigned long long key = ~0ull;
+        if (i < count) {
+            const int64_t v = y[start + i];
+            if (v != ignore_index && v >= 0 && v < V)
+                key = (static_cast<unsigned long long>(v) << 32) |
+                      static_cast<unsigned long long>(start + i - chunk_start);
+        }
+        sk[i] = key;
+    }
+    __syncthreads();
+    for (int size = 2; size <= LABEL_BLOCK; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < LABEL_BLOCK / 2; i += blockDim.x) {
+                const int lo = 2 * i - (i & (stride - 1));
+                const int hi = lo + stride;
+                const bool ascending = (lo & size) == 0;
+                const unsigned long long x0 = sk[lo], x1 = sk[hi];
+                if ((x0 > x1) == ascending) {
+                    sk[lo] = x1;
+                    sk[hi] = x0;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = threadIdx.x; i < LABEL_BLOCK; i += blockDim.x) keys_out[b * LABEL_BLOCK + i] = sk[i];
+}
+
+// The one-hot part of grad_W for one sorted block of a chunk:
+//   grad_W_acc[v, :] -= s * sum over the block's rows i with y_i = v of X[i, :]
+// One CTA per run of equal labels (a CTA whose key does not start a run
+// exits), summing the run's rows in row order in fp32, so the result is the
+// same on every call.  Runs have distinct labels, so no two CTAs touch the
+// same grad_W row.  With write_bf16 the updated rows' bf16 cast is rewritten.
+__global__ void __launch_bounds__(256) onehot_scatter_kernel(const unsigned long long* __restrict__ keys, int64_t n,
+                                                             const uint16_t* __restrict__ X_chunk, int64_t H,
+                                                             const WsHeader* hdr, float* grad_W_acc,
+                                                             uint16_t* grad_W, int write_bf16) {
+    const int64_t p = blockIdx.x;
+    if (p >= n) return;
+    const unsigned long long key = keys[p];
+    if (key == ~0ull) return;
+    const unsigned long long v = key >> 32;
+    if (p > 0 && (keys[p - 1] >> 32) == v) return;
+    int64_t q = p + 1;
+    while (q < n && keys[q] != ~0ull && (keys[q] >> 32) == v) ++q;
+    const float s = hdr->scale;
+    for (int64_t h = static_cast<int64_t>(threadIdx.x) * 8; h < H; h += static_cast<int64_t>(blockDim.x) * 8) {
+        float sum[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sum[k] = 0.f;
+        for (int64_t j = p; j < q; ++j) {
+            const int64_t row = static_cast<int64_t>(keys[j] & 0xFFFFFFFFull);
+            const uint4 w = *reinterpret_cast<const uint4*>(X_chunk + row * H + h);
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                sum[2 * k] += __uint_as_float(u[k] << 16);
+                sum[2 * k + 1] += __uint_as_float(u[k] & 0xFFFF0000u);
+            }
+        }
+        float* acc = grad_W_acc + static_cast<int64_t>(v) * H + h;
+        float4 a0 = *reinterpret_cast<float4*>(acc);
+        float4 a1 = *reinterpret_cast<float4*>(acc + 4);
+        a0.x = fmaf(-s, sum[0], a0.x);
+        a0.y = fmaf(-s, sum[1], a0.y);
+        a0.z = fmaf(-s, sum[2], a0.z);
+        a0.w = fmaf(-s, sum[3], a0.w);
+        a1.x = fmaf(-s, sum[4], a1.x);
+        a1.y = fmaf(-s, sum[5], a1.y);
+        a1.z = fmaf(-s, sum[6], a1.z);
+        a1.w = fmaf(-s, sum[7], a1.w);
+        *reinterpret_cast<float4*>(acc) = a0;
+        *reinterpret_cast<float4*>(acc + 4) = a1;
+        if (write_bf16) {
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(a0.x, a0.y), b1 = __floats2bfloat162_rn(a0.z, a0.w);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(a1.x, a1.y), b3 = __floats2bfloat162_rn(a1.z, a1.w);
+            uint4 o;
+            o.x = *reinterpret_cast<uint32_t*>(&b0);
+            o.y = *reinterpret_cast<uint32_t*>(&b1);
+            o.z = *reinterpret_cast<uint32_t*>(&b2);
+            o.w = *reinterpret_cast<uint32_t*>(&b3);
+            *reinterpret_cast<uint4*>(grad_W + static_cast<int64_t>(v) * H + h) = o;
+        }
+    }
+}
+
+// max |x| over bf16 values, as float bits (non-negative floats order like
+// their bit patterns, so an integer max is exact and order-independent).
+__global__ void amax_kernel(const uint16_t* __restrict__ x, int64_t n, unsigned* amax_bits) {
+    unsigned m = 0;
+    const int64_t n8 = n / 8;
+    const uint4* x8 = reinterpret_cast<const uint4*>(x);
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint4 w = x8[i];
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            m = max(m, (u[k] & 0x7FFFu) << 16);
+            m = max(m, (u[k] >> 16 & 0x7FFFu) << 16);
+        }
+    }
+    for (int64_t i = n8 * 8 + blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        m = max(m, static_cast<unsigned>(x[i] & 0x7FFFu) << 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, m);
+}
+
+// out = fp16(x * 2^k), k = operand_scale_exp(max |x|), round to nearest even.
+__global__ void to_f16_scaled_kernel(const uint16_t* __restrict__ x, int64_t n, const unsigned* amax_bits,
+                                     uint16_t* __restrict__ out) {
+    const float f = ldexpf(1.f, operand_scale_exp(*amax_bits));
+    const int64_t n8 = n / 8;
+    const uint4* x8 = reinterpret_cast<const uint4*>(x);
+    uint4* o8 = reinterpret_cast<uint4*>(out);
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint4 w = x8[i];
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+        uint32_t r[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            __half2 h = __floats2half2_rn(__uint_as_float(u[k] << 16) * f, __uint_as_float(u[k] & 0xFFFF0000u) * f);
+            r[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        o8[i] = make_uint4(r[0], r[1], r[2], r[3]);
+    }
+    for (int64_t i = n8 * 8 + blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        __half h = __float2half_rn(__uint_as_float(static_cast<uint32_t>(x[i]) << 16) * f);
+        out[i] = *reinterpret_cast<uint16_t*>(&h);
+    }
+}
+
+// One thread waits on a barrier nobody signals, with the pipeline's bounded
+// wait; it must come back with the timeout bit set.
+__global__ void wait_probe_kernel(unsigned* status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    fence_barrier_init();
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(b, 0)) {
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicOr(status, STATUS_TIMEOUT);
+            break;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prepass(const int64_t* y, int64_t N, int64_t V, int64_t ignore_index, WsHeader* hdr,
+                           int* label_counts, cudaStream_t s) {
+    const int threads = 256;
+    const int64_t want = (N + threads - 1) / threads;
+    const int blocks = static_cast<int>(want < 1024 ? want : 1024);
+    prepass_kernel<<<blocks, threads, 0, s>>>(y, N, V, ignore_index, hdr, label_counts);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_label_sort(const int64_t* y, int64_t N, int64_t C, int64_t blocks_per_chunk, int64_t n_blocks,
+                              int64_t V, int64_t ignore_index, unsigned long long* keys, cudaStream_t s) {
+    static int configured_device = -1;
+    constexpr int smem = LABEL_BLOCK * 8;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(label_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    label_sort_kernel<<<static_cast<unsigned>(n_blocks), 1024, smem, s>>>(y, N, C, blocks_per_chunk, V,
+                                                                          ignore_index, keys);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_onehot_scatter(const unsigned long long* keys, int64_t n, const uint16_t* X_chunk, int64_t H,
+                                  const WsHeader* hdr, float* grad_W_acc, uint16_t* grad_W, int write_bf16,
+                                  cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    onehot_scatter_kernel<<<static_cast<unsigned>(n), 256, 0, s>>>(keys, n, X_chunk, H, hdr, grad_W_acc, grad_W,
+                                                                   write_bf16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale(WsHeader* hdr, float grad_scale, const float* d_grad_output, int64_t* n_valid_out,
+                         cudaStream_t s) {
+    scale_kernel<<<1, 1, 0, s>>>(hdr, grad_scale, d_grad_output, n_valid_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* part_m, const float* part_s, int64_t n_vt, int64_t ldp, int64_t rows,
+                           const float* zt, const int64_t* y, int64_t ignore_index, float* lse, float* row_loss,
+                           cudaStream_t s) {
+    const int threads = 128;
+    const int64_t blocks = (rows + threads - 1) / threads;
+    combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(part_m, part_s, n_vt, ldp, rows, zt, y,
+                                                                      ignore_index, lse, row_loss);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_loss(const float* row_loss, int64_t N, const WsHeader* hdr, float* loss, int64_t* n_valid_out,
+                        cudaStream_t s) {
+    loss_kernel<<<1, 1024, 0, s>>>(row_loss, N, hdr, loss, n_valid_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_grad_b(const float* gb_part, int64_t parts, int64_t V, const WsHeader* hdr,
+                          const int* label_counts, float* grad_b_acc, uint16_t* grad_b, int first, int last,
+                          cudaStream_t s) {
+    const int threads = 256;
+    const int64_t blocks = (V + threads - 1) / threads;
+    grad_b_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(gb_part, parts, V, hdr, label_counts,
+                                                                     grad_b_acc, grad_b, first, last);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_probe(unsigned* status, uint64_t limit_ns, cudaStream_t s) {
+    wait_probe_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_amax(const uint16_t* x, int64_t n, unsigned* amax_bits, cudaStream_t s) {
+    const int threads = 256;
+    const int64_t want = (n / 8 + threads - 1) / threads;
+    const int blocks = static_cast<int>(want < 1 ? 1 : (want < 2048 ? want : 2048));
+    amax_kernel<<<blocks, threads, 0, s>>>(x, n, amax_bits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_to_f16_scaled(const uint16_t* x, int64_t n, const unsigned* amax_bits, uint16_t* out,
+                                 cudaStream_t s) {
+    const int threads = 256;
+    const int64_t want = (n / 8 + threads - 1) / threads;
+    const int blocks = static_cast<int>(want < 1 ? 1 : (want < 4096 ? want : 4096));
+    to_f16_scaled_kernel<<<blocks, threads, 0, s>>>(x, n, amax_bits, out);
+    return cudaGetLastError();
+}
+
+}  // namespace lce

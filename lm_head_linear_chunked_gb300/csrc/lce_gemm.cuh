@@ -1,0 +1,507 @@
+// The library's one tensor-core GEMM: a persistent, warp-specialised
+// tcgen05 kernel for sm_103a, with one fused epilogue per role.
+//
+//   warp 0 (one lane): TMA producer.  Loads 128x64 A and 256x64 B bf16 slices
+//          (128-byte swizzled) into a 4-stage shared-memory ring.
+//   warp 1 (one lane): MMA issuer.  Four tcgen05.mma (M=128, N=256, K=16)
+//          per slice into one of two 256-column fp32 TMEM accumulators;
+//          tcgen05.commit frees ring slots and publishes finished tiles.
+//   warps 2..5: epilogue.  Each thread owns one accumulator row (its TMEM
+//          lane), reads it 32 columns at a time with tcgen05.ld and applies
+//          the role's epilogue while the MMA warp fills the other buffer.
+//
+// Every wait is bounded (globaltimer); a wait that runs out raises the
+// status bit, flags the CTA to stop, and the CTA drains its in-flight
+// copies and MMAs, frees TMEM and returns.  Nothing traps.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "lce_internal.cuh"
+#include "lce_ptx.cuh"
+
+namespace lce {
+
+constexpr float LOG2E_F = 1.4426950408889634f;
+constexpr float P_SCALE = static_cast<float>(1 << P_SCALE_EXP);
+
+__device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+template <int MODE>
+struct ModeTraits {
+    static constexpr bool A_MN = (MODE == MODE_PLAIN_MM || MODE == MODE_GRADW);
+    static constexpr bool B_MN = (MODE == MODE_PLAIN_KM || MODE == MODE_PLAIN_MM ||
+                                  MODE == MODE_GRADX || MODE == MODE_GRADW);
+    static constexpr bool F16 = (MODE == MODE_GRADX || MODE == MODE_GRADW);
+};
+
+struct SharedCtl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    volatile int abort_flag;
+};
+static_assert(sizeof(SharedCtl) <= CTL_BYTES, "control block too large");
+
+// Waits for the phase of parity `parity` of barrier `bar`.  Gives up, raising
+// the CTA's abort flag and the timeout status bit, after `limit_ns`; with
+// `honor_abort` it also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, SharedCtl* ctl,
+                                           unsigned* status, uint64_t limit_ns,
+                                           bool honor_abort = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (honor_abort && ctl->abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            ctl->abort_flag = 1;
+            atomicOr(status, STATUS_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tile_coords(int t, const GemmArgs& a, int& m, int& n) {
+    if (a.raster == 0) {
+        m = t % a.m_tiles;
+        n = t / a.m_tiles;
+    } else if (a.raster == 1) {
+        n = t % a.n_tiles;
+        m = t / a.n_tiles;
+    } else {
+        const int per = a.group_m * a.n_tiles;
+        const int g = t / per;
+        const int r = t - g * per;
+        const int gm0 = g * a.group_m;
+        const int gm = min(a.group_m, a.m_tiles - gm0);
+        m = gm0 + r % gm;
+        n = r / gm;
+    }
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// Adds b[0 .. nv) (bf16, 16-byte aligned when nv == 32) to v[0 .. nv).
+__device__ __forceinline__ void add_bias32(float (&v)[32], const uint16_t* b, int nv) {
+    if (nv == 32) {
+        const uint4* p = reinterpret_cast<const uint4*>(b);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const uint4 w = __ldg(p + g);
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                v[8 * g + 2 * k] += bf16_bits_to_float(u[k] & 0xFFFFu);
+                v[8 * g + 2 * k + 1] += bf16_bits_to_float(u[k] >> 16);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < nv) v[i] += bf16_bits_to_float(__ldg(b + i));
+    }
+}
+
+// Stores v[0 .. nv) as bf16 (round to nearest even); nv is a multiple of 8.
+__device__ __forceinline__ void store_bf16_32(uint16_t* dst, const float (&v)[32], int nv) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (8 * g < nv) {
+            uint4 w;
+            w.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
+            w.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
+            w.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
+            w.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
+            *reinterpret_cast<uint4*>(dst + 8 * g) = w;
+        }
+    }
+}
+
+// Stores v[0 .. nv) as fp16 (round to nearest even); nv is a multiple of 8.
+__device__ __forceinline__ void store_f16_32(uint16_t* dst, const float (&v)[32], int nv) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (8 * g < nv) {
+            __half2 h[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) h[k] = __floats2half2_rn(v[8 * g + 2 * k], v[8 * g + 2 * k + 1]);
+            uint4 w;
+            w.x = *reinterpret_cast<uint32_t*>(&h[0]);
+            w.y = *reinterpret_cast<uint32_t*>(&h[1]);
+            w.z = *reinterpret_cast<uint32_t*>(&h[2]);
+            w.w = *reinterpret_cast<uint32_t*>(&h[3]);
+            *reinterpret_cast<uint4*>(dst + 8 * g) = w;
+        }
+    }
+}
+
+// Stores v[0 .. nv) as fp32; nv is a multiple of 4.
+__device__ __forceinline__ void store_f32_32(float* dst, const float (&v)[32], int nv) {
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+        if (4 * g < nv)
+            *reinterpret_cast<float4*>(dst + 4 * g) =
+                make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+}
+
+// Sum over the warp's 32 rows of each of 32 columns: afterwards lane k holds
+// the sum of column k.  Five halving exchange steps (16+8+4+2+1 shuffles).
+__device__ __forceinline__ float warp_column_sums(float (&g)[32], int lane) {
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool upper = (lane & w) != 0;
+#pragma unroll
+        for (int k = 0; k < w; ++k) {
+            const float send = upper ? g[k] : g[k + w];
+            const float keep = upper ? g[k + w] : g[k];
+            g[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, w);
+        }
+    }
+    return g[0];
+}
+
+template <int MODE>
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, int q, int lane,
+                                              uint32_t taddr, uint32_t empty_bar) {
+    const int64_t row = static_cast<int64_t>(m) * BM + q * 32 + lane;
+    const int64_t col0 = static_cast<int64_t>(n) * BN;
+    const bool row_ok = row < a.M;
+
+    if constexpr (MODE == MODE_LSE) {
+        const int64_t yr = row_ok ? a.y[row] : a.ignore_index;
+        float mx = -INFINITY, sm = 0.f, zt = 0.f;
+        bool got = false;
+#pragma unroll 1
+        for (int j = 0; j < BN / 32; ++j) {
+            const int64_t c0 = col0 + 32 * j;
+            if (c0 >= a.N) break;
+            float v[32];
+            tmem_load_32cols(taddr + 32 * j, v);
+            const int nv = static_cast<int>(min64(32, a.N - c0));
+            if (a.bias) add_bias32(v, a.bias + c0, nv);
+            const int64_t d = yr - c0;
+            const int kk = (d >= 0 && d < 32) ? static_cast<int>(d) : -1;
+            got |= kk >= 0;
+            float cm = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                zt = (i == kk) ? v[i] : zt;
+                const float t = (i < nv) ? v[i] * LOG2E_F : -INFINITY;
+                v[i] = t;
+                cm = fmaxf(cm, t);
+            }
+            const float mn = fmaxf(mx, cm);
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc += fast_exp2(v[i] - mn);
+            sm = sm * fast_exp2(mx - mn) + acc;
+            mx = mn;
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar);
+        if (row_ok) {
+            a.part_m[static_cast<int64_t>(n) * a.ldp + row] = mx;
+            a.part_s[static_cast<int64_t>(n) * a.ldp + row] = sm;
+            if (got) a.zt[row] = zt;
+        }
+    } else if constexpr (MODE == MODE_G) {
+        const int64_t yr = row_ok ? a.y[row] : a.ignore_index;
+        const bool valid = row_ok && yr != a.ignore_index;
+        const float lse2 = row_ok ? a.lse[row] * LOG2E_F : 0.f;
+#pragma unroll 1
+        for (int j = 0; j < BN / 32; ++j) {
+            const int64_t c0 = col0 + 32 * j;
+            if (c0 >= a.N) break;
+            float v[32];
+            tmem_load_32cols(taddr + 32 * j, v);
+            const int nv = static_cast<int>(min64(32, a.N - c0));
+            if (a.bias) add_bias32(v, a.bias + c0, nv);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float p = fast_exp2(fmaf(v[i], LOG2E_F, -lse2));
+                v[i] = (valid && i < nv) ? p : 0.f;
+            }
+            if (row_ok) {
+                float ps[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) ps[i] = v[i] * P_SCALE;
+                store_f16_32(a.g + row * a.ldg + c0, ps, static_cast<int>(min64(32, a.ldg - c0)));
+            }
+            if (a.gb_part) {
+                const float cs = warp_column_sums(v, lane);
+                if (c0 + lane < a.N) a.gb_part[(static_cast<int64_t>(m) * 4 + q) * a.N + c0 + lane] = cs;
+            }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar);
+    } else if constexpr (MODE == MODE_GRADX) {
+        // grad_X[i] = s (sum_v P[i,v] W[v] - W[y_i]); P rows of ignored rows are 0
+        const float s = *a.scale;
+        const float f = ldexpf(s, -(P_SCALE_EXP + operand_scale_exp(*a.b_amax_bits)));
+        const int64_t yr = row_ok ? a.y[row] : a.ignore_index;
+        const bool valid = row_ok && yr != a.ignore_index && yr >= 0 && yr < a.V;
+        const uint16_t* wy = a.w_rows + (valid ? yr : 0) * a.ldw;
+#pragma unroll 1
+        for (int j = 0; j < BN / 32; ++j) {
+            const int64_t c0 = col0 + 32 * j;
+            if (c0 >= a.N) break;
+            float v[32];
+            tmem_load_32cols(taddr + 32 * j, v);
+            if (row_ok) {
+                if (valid) {
+                    float w[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) w[i] = 0.f;
+                    add_bias32(w, wy + c0, 32);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = fmaf(f, v[i], -s * w[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= f;
+                }
+                store_bf16_32(a.out_bf16 + row * a.ld_out + c0, v, static_cast<int>(min64(32, a.N - c0)));
+            }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar);
+    } else if constexpr (MODE == MODE_GRADW) {
+        const float s = ldexpf(*a.scale, -(P_SCALE_EXP + operand_scale_exp(*a.b_amax_bits)));
+#pragma unroll 1
+        for (int j = 0; j < BN / 32; ++j) {
+            const int64_t c0 = col0 + 32 * j;
+            if (c0 >= a.N) break;
+            float v[32];
+            tmem_load_32cols(taddr + 32 * j, v);
+            if (row_ok) {
+                float* p = a.out_f32 + row * a.ld_f32 + c0;
+                if (a.acc_first) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= s;
+                } else {
+                    float4 old[8];
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) old[g] = *reinterpret_cast<const float4*>(p + 4 * g);
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        v[4 * g + 0] = fmaf(s, v[4 * g + 0], old[g].x);
+                        v[4 * g + 1] = fmaf(s, v[4 * g + 1], old[g].y);
+                        v[4 * g + 2] = fmaf(s, v[4 * g + 2], old[g].z);
+                        v[4 * g + 3] = fmaf(s, v[4 * g + 3], old[g].w);
+                    }
+                }
+                store_f32_32(p, v, 32);
+                if (a.write_bf16) store_bf16_32(a.out_bf16 + row * a.ld_out + c0, v, 32);
+            }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar);
+    } else {  // PLAIN: D = fp32 product
+#pragma unroll 1
+        for (int j = 0; j < BN / 32; ++j) {
+            const int64_t c0 = col0 + 32 * j;
+            if (c0 >= a.N) break;
+            float v[32];
+            tmem_load_32cols(taddr + 32 * j, v);
+            if (row_ok) store_f32_32(a.out_f32 + row * a.ld_f32 + c0, v, static_cast<int>(min64(32, a.N - c0)));
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar);
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                const GemmArgs args) {
+    using T = ModeTraits<MODE>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle needs 1024-byte alignment
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem_raw + (base - raw) + STAGES * STAGE_BYTES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint64_t limit = args.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&ctl->tmem_full[b]), 1);
+            mbar_init(smem_u32(&ctl->tmem_empty[b]), 4);
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&map_a);
+        tma_prefetch_map(&map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const int num_tiles = args.m_tiles * args.n_tiles;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            uint32_t stage = 0, phase = 0;
+            uint64_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                int m, n;
+                tile_coords(t, args, m, n);
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!wait_phase(smem_u32(&ctl->empty[stage]), phase ^ 1u, ctl, args.status, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&ctl->full[stage]);
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    const uint32_t sa = base + stage * STAGE_BYTES;
+                    const uint32_t sb = sa + A_STAGE_BYTES;
+                    const int32_t k0 = kb * BK;
+                    if constexpr (!T::A_MN) {
+                        tma_load_2d(sa, &map_a, fb, k0, args.a_y0 + m * BM);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BM / 64; ++j)
+                            tma_load_2d(sa + j * 8192, &map_a, fb, m * BM + 64 * j, args.a_y0 + k0);
+                    }
+                    if constexpr (!T::B_MN) {
+                        tma_load_2d(sb, &map_b, fb, k0, args.b_y0 + n * BN);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_load_2d(sb + j * 8192, &map_b, fb, n * BN + 64 * j, args.b_y0 + k0);
+                    }
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let the copies still in flight land before the CTA exits.
+                const uint64_t last = issued < STAGES ? issued : STAGES;
+                for (uint64_t i = 0; i < last; ++i) {
+                    const uint64_t j = issued - 1 - i;
+                    wait_phase(smem_u32(&ctl->full[j % STAGES]), static_cast<uint32_t>((j / STAGES) & 1u),
+                               ctl, args.status, limit, false);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t IDESC = instr_desc_f16kind(BM, BN, T::A_MN, T::B_MN, T::F16);
+            // descriptor start-address step per K=16 MMA, in 16-byte units:
+            // K-major: 32 bytes along the swizzled row; MN-major: two 8-row groups.
+            constexpr uint32_t A_STEP = T::A_MN ? (2048u >> 4) : (32u >> 4);
+            constexpr uint32_t B_STEP = T::B_MN ? (2048u >> 4) : (32u >> 4);
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                if (!wait_phase(smem_u32(&ctl->tmem_empty[acc]), acc_phase ^ 1u, ctl, args.status, limit)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!wait_phase(smem_u32(&ctl->full[stage]), phase, ctl, args.status, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = base + stage * STAGE_BYTES;
+                    const uint32_t sb = sa + A_STAGE_BYTES;
+                    const uint64_t adesc = T::A_MN ? smem_desc_sw128(sa, 8192, 1024) : smem_desc_sw128(sa, 16, 1024);
+                    const uint64_t bdesc = T::B_MN ? smem_desc_sw128(sb, 8192, 1024) : smem_desc_sw128(sb, 16, 1024);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        mma_f16kind(d_tmem, adesc + A_STEP * k, bdesc + B_STEP * k, IDESC,
+                                     (kb | k) != 0 ? 1u : 0u);
+                    mma_commit(smem_u32(&ctl->empty[stage]));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&ctl->tmem_full[acc]));
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok) {
+                // Wait for every MMA this thread issued before TMEM is freed.
+                mma_commit(smem_u32(&ctl->drain));
+                wait_phase(smem_u32(&ctl->drain), 0, ctl, args.status, limit, false);
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5; warp w reads TMEM lanes 32*(w%4) ..)
+        const int q = warp & 3;
+        uint32_t acc = 0, acc_phase = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            int m, n;
+            tile_coords(t, args, m, n);
+            if (!wait_phase(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, args.status, limit)) break;
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+            epilogue_tile<MODE>(args, m, n, q, lane, taddr, smem_u32(&ctl->tmem_empty[acc]));
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    __syncwarp();  // reconverge the producer and MMA warps (one lane worked)
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+template <int MODE>
+cudaError_t launch_gemm_mode(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
+                             int grid, cudaStream_t stream) {
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GEMM_SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    gemm_kernel<MODE><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(map_a, map_b, args);
+    return cudaGetLastError();
+}
+
+}  // namespace lce

@@ -1,0 +1,149 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lce.h"
+
+namespace lce {
+
+// Roles of the one tensor-core GEMM kernel.  The three PLAIN modes write the
+// bare fp32 product (diagnostics); the other four are the loss's GEMMs, each
+// with its own fused epilogue.
+enum GemmMode : int {
+    MODE_PLAIN_KK = 0,  // D = A B^T,  A [M,K], B [N,K]        (both K-major)
+    MODE_PLAIN_KM = 1,  // D = A B,    A [M,K], B [K,N]        (B MN-major)
+    MODE_PLAIN_MM = 2,  // D = A^T B,  A [K,M], B [K,N]        (both MN-major)
+    MODE_LSE = 3,       // logits X_c W^T -> per-row partial (max, sum exp), target logit
+    MODE_G = 4,         // logits X_c W^T -> P = softmax (fp16, scaled by 2^P_SCALE_EXP), bias column sums
+    MODE_GRADX = 5,     // grad_X_c = s * (P W - W[y])           (fp16 operands, bf16 out)
+    MODE_GRADW = 6,     // grad_W_acc (+)= s * P^T X_c           (fp16 operands, fp32 accumulator, bf16 cast)
+};
+
+// Tile shape: 128 rows (TMEM lanes) x 256 columns (fp32 TMEM columns),
+// 64-element (128-byte) K slices, a 4-deep shared-memory ring.
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;                 // 16 KB
+constexpr int B_STAGE_BYTES = BN * BK * 2;                 // 32 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES; // 48 KB
+constexpr int CTL_BYTES = 256;
+constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + CTL_BYTES;
+constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr uint32_t TMEM_COLS = 512; // two 256-column fp32 accumulators
+
+// Device status word bits (bit k set = lce_status_t k was raised).
+constexpr unsigned STATUS_LABEL = 1u << LCE_ERR_LABEL_RANGE;
+constexpr unsigned STATUS_TIMEOUT = 1u << LCE_ERR_TIMEOUT;
+
+// The gradient GEMMs take fp16 operands (11 significant bits, against bf16's
+// 8): P is stored as fp16(p * 2^P_SCALE_EXP), and W and X are converted to
+// fp16 with an exact power-of-two scale 2^k chosen from their largest
+// magnitude (k = operand_scale_exp()), so the conversion loses nothing of
+// the bf16 values that matter.  Epilogues undo the scales exactly.
+constexpr int P_SCALE_EXP = 15;
+
+// Rows per block of the label sort that drives the exact one-hot part of
+// grad_W (one CTA sorts one block in shared memory).
+constexpr int LABEL_BLOCK = 8192;
+
+// Default limit of one pipeline wait.  The longest legitimate wait is one
+// tile's main loop (under a millisecond for K = 151936).
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
+
+// First 256 bytes of every workspace.
+struct WsHeader {
+    unsigned status;
+    unsigned pad0;
+    unsigned long long n_valid;
+    float scale;          // s = grad_scale * grad_output / n_valid (0 if n_valid == 0)
+    unsigned amax_x_bits; // float bits of max |X|
+    unsigned amax_w_bits; // float bits of max |W|
+    unsigned pad1;
+};
+
+// Exponent k with amax * 2^k < 2^15 (so every |value| * 2^k fits fp16's
+// range with room to spare); 0 for a zero or non-finite amax.
+__host__ __device__ inline int operand_scale_exp(unsigned amax_bits) {
+    const int e = static_cast<int>((amax_bits >> 23) & 0xFFu);
+    if (e == 0 || e == 255) return 0;
+    return 141 - e;  // amax < 2^(e - 126)
+}
+
+struct GemmArgs {
+    int32_t m_tiles, n_tiles, k_blocks;
+    int32_t raster;   // 0: m fastest, 1: n fastest, 2: groups of group_m m-tiles
+    int32_t group_m;
+    int32_t a_y0;     // added to A's outer (row) TMA coordinate
+    int32_t b_y0;     // added to B's outer (row) TMA coordinate
+    int64_t M, N;     // valid extent of the output (rows, columns)
+    // MODE_LSE / MODE_G
+    const int64_t* y;  // labels of this chunk's first row
+    int64_t ignore_index;
+    const uint16_t* bias;  // nullable
+    float* part_m;     // [n_tiles, ldp] per-row running max (base-2 units)
+    float* part_s;     // [n_tiles, ldp] per-row sum of 2^(t - max)
+    float* zt;         // [chunk rows] target logit
+    int64_t ldp;
+    const float* lse;  // this chunk's first row
+    uint16_t* g;       // P [chunk rows, ldg] bf16
+    int64_t ldg;
+    float* gb_part;    // [m_tiles * 4, V] column sums of P (nullable)
+    // MODE_GRADX: the one-hot part, -W[y_i], is applied exactly in the epilogue
+    const uint16_t* w_rows;
+    int64_t ldw;
+    int64_t V;
+    // MODE_GRADX / MODE_GRADW: float bits of max |B operand| (its fp16 scale)
+    const unsigned* b_amax_bits;
+    // MODE_GRADX / MODE_GRADW / PLAIN
+    const float* scale;  // device scalar s
+    uint16_t* out_bf16;
+    int64_t ld_out;
+    float* out_f32;
+    int64_t ld_f32;
+    int32_t acc_first;   // MODE_GRADW: overwrite instead of accumulate
+    int32_t write_bf16;  // MODE_GRADW: also write the bf16 cast
+    unsigned* status;
+    uint64_t timeout_ns;
+};
+
+// Launches the GEMM kernel of `mode`.  The instantiations are spread over
+// three translation units so that they compile in parallel.
+cudaError_t launch_gemm(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                        const GemmArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_logits(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                               const GemmArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_grads(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                              const GemmArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_plain(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                              const GemmArgs& args, int grid, cudaStream_t stream);
+
+// Small kernels (lce_aux.cu).
+cudaError_t launch_prepass(const int64_t* y, int64_t N, int64_t V, int64_t ignore_index,
+                           WsHeader* hdr, int* label_counts, cudaStream_t s);
+cudaError_t launch_label_sort(const int64_t* y, int64_t N, int64_t C, int64_t blocks_per_chunk,
+                              int64_t n_blocks, int64_t V, int64_t ignore_index,
+                              unsigned long long* keys, cudaStream_t s);
+cudaError_t launch_onehot_scatter(const unsigned long long* keys, int64_t n, const uint16_t* X_chunk,
+                                  int64_t H, const WsHeader* hdr, float* grad_W_acc,
+                                  uint16_t* grad_W, int write_bf16, cudaStream_t s);
+cudaError_t launch_scale(WsHeader* hdr, float grad_scale, const float* d_grad_output,
+                         int64_t* n_valid_out, cudaStream_t s);
+cudaError_t launch_combine(const float* part_m, const float* part_s, int64_t n_vt, int64_t ldp,
+                           int64_t rows, const float* zt, const int64_t* y, int64_t ignore_index,
+                           float* lse, float* row_loss, cudaStream_t s);
+cudaError_t launch_loss(const float* row_loss, int64_t N, const WsHeader* hdr, float* loss,
+                        int64_t* n_valid_out, cudaStream_t s);
+cudaError_t launch_grad_b(const float* gb_part, int64_t parts, int64_t V, const WsHeader* hdr,
+                          const int* label_counts, float* grad_b_acc, uint16_t* grad_b, int first,
+                          int last, cudaStream_t s);
+cudaError_t launch_wait_probe(unsigned* status, uint64_t limit_ns, cudaStream_t s);
+cudaError_t launch_amax(const uint16_t* x, int64_t n, unsigned* amax_bits, cudaStream_t s);
+cudaError_t launch_to_f16_scaled(const uint16_t* x, int64_t n, const unsigned* amax_bits, uint16_t* out,
+                                 cudaStream_t s);
+
+}  // namespace lce

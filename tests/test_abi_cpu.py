@@ -1,0 +1,133 @@
+"""The C ABI without a GPU: the library loads, exports every entry point
+include/lce.h declares, sizes workspaces, and rejects bad arguments on the
+host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+import lm_head_linear_chunked_gb300 as lce
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lce.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    __graft_entry__.build()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"LCE_API\s+[\w\s\*]*?\b(lce_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for n in ("lce_workspace_size", "lce_forward", "lce_backward", "lce_fused_fwd_bwd", "lce_check_status",
+              "lce_status_string", "lce_chunk_rows", "lce_debug_gemm", "lce_debug_wait_timeout"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = ctypes.CDLL(lce.library_path)
+    for n in declared_symbols():
+        assert hasattr(L, n), n
+    assert set(declared_symbols()) <= set(lce._SIGS)
+
+
+def test_status_strings():
+    for code, name in lce.STATUS.items():
+        assert lce.lce_status_string(code)
+    assert lce.lce_status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("N,chunk,expect", [(512, 256, 256), (512, 0, 512), (100000, 0, 8192), (7, 1000, 7),
+                                            (131072, 0, 8192), (4096, 1, 1)])
+def test_chunk_rows(N, chunk, expect):
+    assert lce.lce_chunk_rows(N, 1024, 32768, chunk) == expect
+
+
+def test_workspace_sizes():
+    N, H, V = 131072, 4096, 151936
+    f = lce.lce_workspace_size(N, H, V, 0, False, lce.WS_FORWARD)
+    b = lce.lce_workspace_size(N, H, V, 0, False, lce.WS_BACKWARD)
+    fb = lce.lce_workspace_size(N, H, V, 0, False, lce.WS_FUSED)
+    assert fb >= max(f, b) and fb <= f + b
+    assert b >= 8192 * V * 2                       # one chunk of bf16 G
+    assert fb < N * V * 2 / 10                     # far below the logits it replaces
+    with_bias = lce.lce_workspace_size(N, H, V, 0, True, lce.WS_FUSED)
+    assert with_bias > fb
+    assert lce.lce_workspace_size(N, H, V, 256, False, lce.WS_FUSED) < fb
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 64, 10, 0), 1), ((10, 64, 0, 0), 1), ((10, 0, 10, 0), 1), ((10, 64, 10, -1), 1),
+    ((10, 100, 10, 0), 2), ((10, 32, 10, 0), 2), ((2**31, 64, 10, 0), 2),
+])
+def test_workspace_size_rejects(args, code):
+    with pytest.raises(lce.LCEError) as e:
+        lce.lce_workspace_size(*args, False, lce.WS_FUSED)
+    assert e.value.status == code
+
+
+def test_workspace_which_is_checked():
+    with pytest.raises(lce.LCEError) as e:
+        lce.lce_workspace_size(10, 64, 10, 0, False, 7)
+    assert e.value.status == 1
+
+
+# Fake, aligned, never-dereferenced addresses: these calls must return before
+# any CUDA work, so they run without a GPU.
+A = 1 << 20
+
+
+def fwd(**kw):
+    args = dict(N=16, H=64, V=32, X=A, W=A, b=None, y=A, ignore_index=-100, chunk_rows=0, loss=A, lse=A,
+                n_valid=None, ws=A, ws_bytes=1 << 30, stream=None)
+    args.update(kw)
+    lce.lce_forward(*args.values())
+
+
+def bwd(**kw):
+    args = dict(N=16, H=64, V=32, X=A, W=A, b=None, y=A, ignore_index=-100, chunk_rows=0, lse=A, grad_scale=1.0,
+                d_grad_output=None, grad_X=A, grad_W=A, grad_b=None, grad_W_acc=A, grad_b_acc=None, ws=A,
+                ws_bytes=1 << 30, stream=None)
+    args.update(kw)
+    lce.lce_backward(*args.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(X=None), 1), (dict(W=None), 1), (dict(y=None), 1), (dict(lse=None), 1), (dict(loss=None), 1),
+    (dict(ws=None), 1), (dict(X=A + 2), 1), (dict(ws=A + 16), 1), (dict(ws_bytes=100), 3),
+    (dict(N=-3), 1), (dict(H=65), 2), (dict(chunk_rows=-5), 1),
+])
+def test_forward_host_errors(kw, code):
+    with pytest.raises(lce.LCEError) as e:
+        fwd(**kw)
+    assert e.value.status == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(grad_W_acc=None), 1), (dict(grad_b=A), 1), (dict(grad_b_acc=A), 1), (dict(b=A), 1),
+    (dict(grad_W=A + 8), 1), (dict(ws_bytes=1000), 3),
+])
+def test_backward_host_errors(kw, code):
+    with pytest.raises(lce.LCEError) as e:
+        bwd(**kw)
+    assert e.value.status == code
+
+
+def test_debug_entry_points_host_errors():
+    with pytest.raises(lce.LCEError) as e:
+        lce.lce_debug_gemm(3, 128, 128, 64, A, A, A, A, 4096, None)
+    assert e.value.status == 1
+    with pytest.raises(lce.LCEError) as e:
+        lce.lce_debug_gemm(0, 128, 100, 64, A, A, A, A, 4096, None)
+    assert e.value.status == 2
+    with pytest.raises(lce.LCEError) as e:
+        lce.lce_debug_wait_timeout(10, A, 8, None)
+    assert e.value.status == 3
+    assert lce.lce_check_status(None, None) == 1
