@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Benchmark of the fused chunked linear cross-entropy forward+backward.
+
+One step = one lce_fused_fwd_bwd call (loss, lse, grad_X, grad_W) on the
+Qwen3-8B head shape: N = 131072 rows (one sequence), H = 4096, V = 151936,
+no bias, labels Zipf(1.1) with 5% ignored, chunk size chosen by the library.
+Inputs are seeded synthetic draws of that shape (lce_inputs).
+
+Prints one JSON line:
+  value     tokens/s with the inputs already resident in HBM (device-timed,
+            CUDA events on the call's stream, W warm-up steps, then K steps)
+  e2e       the same metric with the inputs in pinned host memory: each step
+            copies X, W, y to the device, runs the call, and copies loss, lse,
+            grad_X and grad_W back, all inside the timed region
+  roofline  the dominant kernel (by device time) against the measured tensor
+            peak: algorithmic FLOPs per launch / mean launch duration, timed
+            live with the library's per-kernel events over the timed region
+  cpu_baseline  the FP64 CPU oracle on a bounded sample of the same rows
+  clocks    nvidia-smi SM clock samples taken during the timed region
+
+`--impl reference` times the FP64 CPU oracle instead, on the host cores,
+each step a bounded sample of the same workload (the oracle is the only
+reference this method has).  With several GPUs (torchrun), every rank runs
+its own replica of the whole workload; value is the sum over ranks of rows
+processed divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+# The oracle's BLAS uses every host core; must be set before numpy loads.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s fused LCE fwd+bwd (Qwen3-8B head) and % of BF16 tensor peak"
+WORKLOAD = "qwen3-8b-head-N131072-H4096-V151936"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w, rows: int, X=None, W_bits=None, y=None):
+    """Runs the FP64 oracle, as it stands, on the first `rows` rows of the
+    workload (all of W): returns (seconds, rows)."""
+    import numpy as np
+
+    import lce_inputs as L
+    import oracle
+
+    if W_bits is None:
+        W_bits = np.empty((w.V, w.H), dtype=np.uint16)
+        L.w_into(w, W_bits.ctypes.data)
+    if y is None:
+        y = L.labels(w)
+    Xr = L.x_rows(w, np.arange(rows))
+    t0 = time.perf_counter()
+    oracle.fused(Xr, W_bits, None, y[:rows])
+    return time.perf_counter() - t0, rows
+
+
+def cpu_baseline(w, rows=256):
+    import numpy as np
+
+    import lce_inputs as L
+    W_bits = np.empty((w.V, w.H), dtype=np.uint16)
+    L.w_into(w, W_bits.ctypes.data)
+    y = L.labels(w)
+    t, n = oracle_sample(w, rows, W_bits=W_bits, y=y)
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": n / t, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"FP64 oracle forward+backward (numpy, float64 BLAS) on the first {n} of {w.N} rows "
+                      f"with all of W [{w.V}x{w.H}], {t:.1f} s"}
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import lce_inputs as L
+    W_bits = np.empty((w.V, w.H), dtype=np.uint16)
+    L.w_into(w, W_bits.ctypes.data)
+    y = L.labels(w)
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample(w, rows, W_bits=W_bits, y=y)
+    times = []
+    for _ in range(args.steps):
+        t, _n = oracle_sample(w, rows, W_bits=W_bits, y=y)
+        times.append(t)
+    t_step = sum(times) / len(times)
+    value = rows / t_step
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: FP64 oracle forward+backward on the first {rows} of {w.N} rows "
+                                   f"with all of W"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.tmp is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == len(self.FIELDS):
+                    rows.append(parts)
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        pw = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"],
+                                 r[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- our library
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import lce_inputs as L
+    import lm_head_linear_chunked_gb300 as lce
+
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    __graft_entry__.build()
+
+    N, H, V = w.N, w.H, w.V
+    chunk = args.chunk_rows if args.chunk_rows is not None else w.chunk_rows
+    # seeded inputs, generated on the host into pinned memory
+    Xh = torch.empty((N, H), dtype=torch.bfloat16, pin_memory=True)
+    Wh = torch.empty((V, H), dtype=torch.bfloat16, pin_memory=True)
+    L.x_into(w, Xh.data_ptr())
+    L.w_into(w, Wh.data_ptr())
+    yh = torch.from_numpy(L.labels(w)).pin_memory()
+
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        X = Xh.to(dev, non_blocking=True)
+        W = Wh.to(dev, non_blocking=True)
+        y = yh.to(dev, non_blocking=True)
+        nws = lce.lce_workspace_size(N, H, V, chunk, False, lce.WS_FUSED)
+        ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+        n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+        gX = torch.empty_like(X)
+        gW = torch.empty_like(W)
+        gW_acc = torch.empty((V, H), dtype=torch.float32, device=dev)
+    s.synchronize()
+
+    def step():
+        lce.lce_fused_fwd_bwd(N, H, V, X, W, None, y, -100, chunk, 1.0, None, loss, lse, n_valid, gX, gW, None,
+                              gW_acc, None, ws, nws, s)
+
+    def barrier():
+        if ws_n > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    st = lce.lce_check_status(ws, s)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {lce.STATUS[st]}")
+
+    # ---- device-resident timing (with per-kernel events)
+    barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        lce.lce_profile_begin()
+        ev0.record(s)
+        for _ in range(args.steps):
+            step()
+        ev1.record(s)
+        torch.cuda.synchronize(dev)
+        prof = lce.lce_profile_end()
+    barrier()
+    clocks = clk.summary()
+    t_step = ev0.elapsed_time(ev1) / 1e3 / args.steps
+    st = lce.lce_check_status(ws, s)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {lce.STATUS[st]}")
+    if ws_n > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([t_step], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step = float(tt.item())
+
+    # ---- end to end: host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        lse_h = torch.empty(N, dtype=torch.float32, pin_memory=True)
+        loss_h = torch.empty(1, dtype=torch.float32, pin_memory=True)
+        gX_h = torch.empty((N, H), dtype=torch.bfloat16, pin_memory=True)
+        gW_h = torch.empty((V, H), dtype=torch.bfloat16, pin_memory=True)
+
+        def e2e_step():
+            with torch.cuda.stream(s):
+                X.copy_(Xh, non_blocking=True)
+                W.copy_(Wh, non_blocking=True)
+                y.copy_(yh, non_blocking=True)
+                step()
+                loss_h.copy_(loss, non_blocking=True)
+                lse_h.copy_(lse, non_blocking=True)
+                gX_h.copy_(gX, non_blocking=True)
+                gW_h.copy_(gW, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(s)
+        torch.cuda.synchronize(dev)
+        barrier()
+        t_e2e = e0.elapsed_time(e1) / 1e3 / args.steps
+        if ws_n > 1:
+            import torch.distributed as dist
+            tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            t_e2e = float(tt.item())
+        h2d = Xh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 8
+        d2h = 4 + N * 4 + gX_h.numel() * 2 + gW_h.numel() * 2
+        e2e = {"value": ws_n * N / t_e2e, "unit": "tokens/s", "ms_per_step": 1e3 * t_e2e,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "path": "lce_fused_fwd_bwd via the Python binding, pinned host buffers"}
+        loss_v = float(loss_h.item())
+    else:
+        loss_v = float(loss.item())
+
+    if rank != 0:
+        if ws_n > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    flops = w.flops_fused()
+    tflops = flops / t_step / 1e12
+    C = lce.lce_chunk_rows(N, H, V, chunk)
+    n_chunks = -(-N // C)
+    # dominant kernel: the GEMM role with the most device time; each launch
+    # does 2 * rows * H * V FLOPs
+    gemm_kinds = ["logits_lse", "logits_softmax", "grad_x", "grad_w"]
+    dom = max(gemm_kinds, key=lambda k: prof[k][0])
+    dom_ms, dom_n = prof[dom]
+    dom_flops_per_launch = 2.0 * N * H * V / n_chunks
+    dom_tflops = dom_flops_per_launch / (dom_ms / dom_n / 1e3) / 1e12
+    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    total_launches = sum(v[1] for v in prof.values())
+    line = {
+        "metric": METRIC, "value": ws_n * N / t_step, "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "N": N, "H": H, "V": V, "chunk_rows": C, "chunks": n_chunks,
+                   "bias": False, "ignored_rows": int((yh == -100).sum().item()),
+                   "l2": "inputs larger than L2 (X 1.07 GB, W 1.24 GB; L2 129 MB)",
+                   "parallelism": "replicas" if ws_n > 1 else "single GPU"},
+        "tflops": tflops,
+        "flops_per_step": flops,
+        "frac_of_peak": {"measured_burst_bf16": tflops / burst, "measured_sustained_bf16": tflops / sustained,
+                         "nominal_dense_bf16_2250": tflops / 2250.0, "peak_source": peak_src},
+        "roofline": {"bound": "tensor", "achieved": dom_tflops, "peak": sustained, "unit": "TFLOP/s",
+                     "frac": dom_tflops / sustained, "traffic": None, "kernel": f"gemm_kernel ({dom})",
+                     "flops_per_launch": dom_flops_per_launch, "launches": dom_n,
+                     "mean_launch_ms": dom_ms / dom_n,
+                     "peak_source": f"{peak_src} sustained bf16 (fp16 operands run at the bf16 rate)"},
+        "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
+        "gpu_launches": total_launches,
+        "loss": loss_v,
+        "workspace_bytes": nws,
+        "logits_bytes_avoided": N * V * 2,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and ws_n == 1:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_rows)
+    print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--chunk-rows", type=int, default=None)
+    ap.add_argument("--cpu-rows", type=int, default=256, help="rows of the CPU-oracle baseline sample")
+    ap.add_argument("--ref-rows", type=int, default=32, help="rows per step of --impl reference")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    import lce_inputs as L
+    w = L.BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

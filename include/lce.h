@@ -167,6 +167,20 @@ LCE_API lce_status_t lce_debug_gemm(int layout, int64_t M, int64_t N, int64_t K,
 LCE_API lce_status_t lce_debug_wait_timeout(uint32_t limit_us, void* ws, size_t ws_bytes,
                                     lce_stream_t stream);
 
+/* Per-kernel device time, for benchmarks.  Between lce_profile_begin() and
+ * lce_profile_end(), every kernel the library enqueues is bracketed by two
+ * CUDA events recorded on the call's own stream (events are created on
+ * first use and kept; no device memory is allocated).  lce_profile_end()
+ * waits for those events and writes, for each kind k < LCE_PROFILE_KINDS,
+ * the summed milliseconds ms[k] and the number of launches launches[k]:
+ *   0 forward logits + logsumexp     1 backward logits -> softmax P
+ *   2 grad_X product                 3 grad_W product
+ *   4 all other (label checks, combine, conversions, one-hot part, loss)
+ * Process-wide state: not for concurrent use from several threads. */
+#define LCE_PROFILE_KINDS 5
+LCE_API lce_status_t lce_profile_begin(void);
+LCE_API lce_status_t lce_profile_end(double* ms, int64_t* launches);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,6 +23,7 @@ __all__ = [
     "LCEError", "IGNORE_INDEX", "WS_FORWARD", "WS_BACKWARD", "WS_FUSED", "STATUS", "library_path", "lib",
     "lce_workspace_size", "lce_chunk_rows", "lce_forward", "lce_backward", "lce_fused_fwd_bwd",
     "lce_check_status", "lce_status_string", "lce_debug_gemm", "lce_debug_wait_timeout",
+    "lce_profile_begin", "lce_profile_end", "PROFILE_KINDS",
     "workspace", "forward", "backward", "fused",
 ]
 
@@ -54,7 +55,11 @@ _SIGS = {
     "lce_status_string": [_STATUS],
     "lce_debug_gemm": [ctypes.c_int, _I64, _I64, _I64, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "lce_debug_wait_timeout": [ctypes.c_uint32, _P, ctypes.c_size_t, _P],
+    "lce_profile_begin": [],
+    "lce_profile_end": [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64)],
 }
+
+PROFILE_KINDS = ("logits_lse", "logits_softmax", "grad_x", "grad_w", "other")
 
 
 class LCEError(RuntimeError):
@@ -156,6 +161,18 @@ def lce_debug_gemm(layout, M, N, K, A, B, D, ws, ws_bytes, stream) -> None:
 
 def lce_debug_wait_timeout(limit_us, ws, ws_bytes, stream) -> None:
     _check(lib().lce_debug_wait_timeout(limit_us, _ptr(ws), ws_bytes, _stream(stream)), "lce_debug_wait_timeout")
+
+
+def lce_profile_begin() -> None:
+    _check(lib().lce_profile_begin(), "lce_profile_begin")
+
+
+def lce_profile_end() -> dict:
+    """{kind: (milliseconds, launches)} of the kernels enqueued since lce_profile_begin()."""
+    ms = (ctypes.c_double * len(PROFILE_KINDS))()
+    n = (_I64 * len(PROFILE_KINDS))()
+    _check(lib().lce_profile_end(ms, n), "lce_profile_end")
+    return {k: (ms[i], n[i]) for i, k in enumerate(PROFILE_KINDS)}
 
 
 # ---------------------------------------------------------------- torch conveniences

@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <vector>
 
 #include "lce_internal.cuh"
 
@@ -140,6 +141,53 @@ GemmArgs base_args(WsHeader* hdr) {
         if ((expr) != cudaSuccess) return LCE_ERR_CUDA; \
     } while (0)
 
+// ---------------------------------------------------------------- profiling
+
+enum ProfKind { PK_LSE = 0, PK_P = 1, PK_GRADX = 2, PK_GRADW = 3, PK_OTHER = 4 };
+
+struct Profiler {
+    std::mutex mu;
+    bool on = false;
+    std::vector<cudaEvent_t> events;  // pairs (start, stop)
+    std::vector<int> kinds;
+    size_t used = 0;
+};
+
+Profiler& profiler() {
+    static Profiler p;
+    return p;
+}
+
+// Records the start event of a profiled launch; returns its slot or -1.
+long prof_start(cudaStream_t s, int kind) {
+    Profiler& p = profiler();
+    if (!p.on) return -1;
+    if (2 * p.used + 2 > p.events.size()) {
+        for (int i = 0; i < 2; ++i) {
+            cudaEvent_t e;
+            if (cudaEventCreate(&e) != cudaSuccess) return -1;
+            p.events.push_back(e);
+        }
+    }
+    const size_t slot = p.used++;
+    if (p.kinds.size() < p.used) p.kinds.resize(p.used);
+    p.kinds[slot] = kind;
+    cudaEventRecord(p.events[2 * slot], s);
+    return static_cast<long>(slot);
+}
+
+void prof_stop(cudaStream_t s, long slot) {
+    if (slot >= 0) cudaEventRecord(profiler().events[2 * slot + 1], s);
+}
+
+#define LCE_LAUNCH(kind, expr)                       \
+    do {                                             \
+        const long slot_ = prof_start(s, (kind));    \
+        const cudaError_t e_ = (expr);               \
+        prof_stop(s, slot_);                         \
+        if (e_ != cudaSuccess) return LCE_ERR_CUDA;  \
+    } while (0)
+
 // ---------------------------------------------------------------- the loss
 
 struct Problem {
@@ -204,15 +252,15 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
 
     LCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
     if (counts) LCE_TRY_CUDA(cudaMemsetAsync(counts, 0, static_cast<size_t>(pb.V) * 4, s));
-    LCE_TRY_CUDA(launch_prepass(pb.y, pb.N, pb.V, pb.ignore_index, hdr, counts, s));
+    LCE_LAUNCH(PK_OTHER, launch_prepass(pb.y, pb.N, pb.V, pb.ignore_index, hdr, counts, s));
     if (do_bwd) {
-        LCE_TRY_CUDA(launch_scale(hdr, o.grad_scale, o.d_grad_output, nullptr, s));
-        LCE_TRY_CUDA(launch_label_sort(pb.y, pb.N, p.C, p.label_blocks_per_chunk,
+        LCE_LAUNCH(PK_OTHER, launch_scale(hdr, o.grad_scale, o.d_grad_output, nullptr, s));
+        LCE_LAUNCH(PK_OTHER, launch_label_sort(pb.y, pb.N, p.C, p.label_blocks_per_chunk,
                                        p.n_chunks * p.label_blocks_per_chunk, pb.V, pb.ignore_index, keys, s));
         // fp16 operands of the gradient GEMMs, with exact power-of-two scales
-        LCE_TRY_CUDA(launch_amax(pb.X, pb.N * pb.H, &hdr->amax_x_bits, s));
-        LCE_TRY_CUDA(launch_amax(pb.W, pb.V * pb.H, &hdr->amax_w_bits, s));
-        LCE_TRY_CUDA(launch_to_f16_scaled(pb.W, pb.V * pb.H, &hdr->amax_w_bits, W16, s));
+        LCE_LAUNCH(PK_OTHER, launch_amax(pb.X, pb.N * pb.H, &hdr->amax_x_bits, s));
+        LCE_LAUNCH(PK_OTHER, launch_amax(pb.W, pb.V * pb.H, &hdr->amax_w_bits, s));
+        LCE_LAUNCH(PK_OTHER, launch_to_f16_scaled(pb.W, pb.V * pb.H, &hdr->amax_w_bits, W16, s));
     }
 
     for (int64_t c = 0; c < p.n_chunks; ++c) {
@@ -235,8 +283,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             a.part_s = ps;
             a.zt = zt;
             a.ldp = p.C;
-            LCE_TRY_CUDA(launch_gemm(MODE_LSE, mX_k, mW_k, a, grid_for(mt * p.n_vt), s));
-            LCE_TRY_CUDA(launch_combine(pm, ps, p.n_vt, p.C, rows, zt, pb.y + r0, pb.ignore_index, o.lse + r0,
+            LCE_LAUNCH(PK_LSE, launch_gemm(MODE_LSE, mX_k, mW_k, a, grid_for(mt * p.n_vt), s));
+            LCE_LAUNCH(PK_OTHER, launch_combine(pm, ps, p.n_vt, p.C, rows, zt, pb.y + r0, pb.ignore_index, o.lse + r0,
                                         row_loss + r0, s));
         }
         if (do_bwd) {
@@ -257,12 +305,12 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.g = G;
                 a.ldg = p.ldg;
                 a.gb_part = gb;
-                LCE_TRY_CUDA(launch_gemm(MODE_G, mX_k, mW_k, a, grid_for(mt * p.n_vt), s));
+                LCE_LAUNCH(PK_P, launch_gemm(MODE_G, mX_k, mW_k, a, grid_for(mt * p.n_vt), s));
             }
             if (gb)
-                LCE_TRY_CUDA(launch_grad_b(gb, mt * 4, pb.V, hdr, counts, o.grad_b_acc, o.grad_b, first, last, s));
+                LCE_LAUNCH(PK_OTHER, launch_grad_b(gb, mt * 4, pb.V, hdr, counts, o.grad_b_acc, o.grad_b, first, last, s));
             // P and X_c maps bounded to this chunk's rows: rows past it read as zero
-            LCE_TRY_CUDA(launch_to_f16_scaled(pb.X + r0 * pb.H, rows * pb.H, &hdr->amax_x_bits, X16, s));
+            LCE_LAUNCH(PK_OTHER, launch_to_f16_scaled(pb.X + r0 * pb.H, rows * pb.H, &hdr->amax_x_bits, X16, s));
             CUtensorMap mG_k, mG_mn, mX16_mn;
             if (!map_16bit_2d(&mG_k, G, rows, pb.V, p.ldg, 64, BM, true) ||
                 !map_16bit_2d(&mG_mn, G, rows, pb.V, p.ldg, 64, 64, true) ||
@@ -286,7 +334,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.ldw = pb.H;
                 a.V = pb.V;
                 a.b_amax_bits = &hdr->amax_w_bits;
-                LCE_TRY_CUDA(launch_gemm(MODE_GRADX, mG_k, mW16_mn, a, grid_for(static_cast<int64_t>(a.m_tiles) * a.n_tiles), s));
+                LCE_LAUNCH(PK_GRADX, launch_gemm(MODE_GRADX, mG_k, mW16_mn, a, grid_for(static_cast<int64_t>(a.m_tiles) * a.n_tiles), s));
             }
             {   // grad_W_acc (+)= s P^T X_c
                 GemmArgs a = base_args(hdr);
@@ -304,19 +352,19 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.acc_first = first;
                 a.write_bf16 = last && o.grad_W != nullptr;
                 a.b_amax_bits = &hdr->amax_x_bits;
-                LCE_TRY_CUDA(launch_gemm(MODE_GRADW, mG_mn, mX16_mn, a, grid_for(static_cast<int64_t>(a.m_tiles) * a.n_tiles), s));
+                LCE_LAUNCH(PK_GRADW, launch_gemm(MODE_GRADW, mG_mn, mX16_mn, a, grid_for(static_cast<int64_t>(a.m_tiles) * a.n_tiles), s));
             }
             // grad_W_acc[y_i] -= s X[i] for the chunk's valid rows, exactly, in row order
             for (int64_t k = 0; k < p.label_blocks_per_chunk; ++k) {
                 const int64_t n = rows - k * LABEL_BLOCK;
                 if (n <= 0) break;
-                LCE_TRY_CUDA(launch_onehot_scatter(keys + (c * p.label_blocks_per_chunk + k) * LABEL_BLOCK,
+                LCE_LAUNCH(PK_OTHER, launch_onehot_scatter(keys + (c * p.label_blocks_per_chunk + k) * LABEL_BLOCK,
                                                    n < LABEL_BLOCK ? n : LABEL_BLOCK, pb.X + r0 * pb.H, pb.H, hdr,
                                                    o.grad_W_acc, o.grad_W, last && o.grad_W != nullptr, s));
             }
         }
     }
-    if (do_fwd) LCE_TRY_CUDA(launch_loss(row_loss, pb.N, hdr, o.loss, o.n_valid, s));
+    if (do_fwd) LCE_LAUNCH(PK_OTHER, launch_loss(row_loss, pb.N, hdr, o.loss, o.n_valid, s));
     return LCE_OK;
 }
 
@@ -431,6 +479,34 @@ const char* lce_status_string(lce_status_t status) {
         case LCE_ERR_CUDA: return "CUDA error";
         default: return "unknown status";
     }
+}
+
+lce_status_t lce_profile_begin(void) {
+    Profiler& p = profiler();
+    std::lock_guard<std::mutex> g(p.mu);
+    p.on = true;
+    p.used = 0;
+    return LCE_OK;
+}
+
+lce_status_t lce_profile_end(double* ms, int64_t* launches) {
+    if (!ms || !launches) return LCE_ERR_INVALID_ARG;
+    Profiler& p = profiler();
+    std::lock_guard<std::mutex> g(p.mu);
+    p.on = false;
+    for (int k = 0; k < LCE_PROFILE_KINDS; ++k) {
+        ms[k] = 0.0;
+        launches[k] = 0;
+    }
+    for (size_t i = 0; i < p.used; ++i) {
+        if (cudaEventSynchronize(p.events[2 * i + 1]) != cudaSuccess) return LCE_ERR_CUDA;
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, p.events[2 * i], p.events[2 * i + 1]) != cudaSuccess) return LCE_ERR_CUDA;
+        ms[p.kinds[i]] += t;
+        launches[p.kinds[i]] += 1;
+    }
+    p.used = 0;
+    return LCE_OK;
 }
 
 lce_status_t lce_debug_gemm(int layout, int64_t M, int64_t N, int64_t K, const lce_bf16* A, const lce_bf16* B,
