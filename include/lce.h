@@ -167,6 +167,36 @@ LCE_API lce_status_t lce_debug_gemm(int layout, int64_t M, int64_t N, int64_t K,
 LCE_API lce_status_t lce_debug_wait_timeout(uint32_t limit_us, void* ws, size_t ws_bytes,
                                     lce_stream_t stream);
 
+/* lce_forward without a caller-provided workspace, for callers that cannot
+ * allocate device memory: for example a hook running inside a framework
+ * whose allocator owns all of the device's memory, or a C client that links
+ * only this library and has no allocator of its own.  (The pages have no
+ * counterpart: their plugin lets PyTorch allocate.)
+ * Arguments and results are those of lce_forward.  The scratch is one
+ * fixed array of LCE_STATIC_SCRATCH_BYTES (32 MiB) in the library's device
+ * memory, reserved on every GPU that loads the library until the process
+ * exits; this call allocates nothing (no cudaMalloc, no cudaFree).
+ * Limits: the forward workspace (lce_workspace_size with LCE_WS_FORWARD)
+ * must fit the array.  With chunk_rows == 0 the largest chunk that fits
+ * is used (at most 8192 rows); a given chunk_rows whose workspace does not
+ * fit, or a problem that does not fit even with one-row chunks (e.g. N
+ * above about eight million rows), returns LCE_ERR_WORKSPACE before
+ * anything is enqueued.
+ * The first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress), so make that first call before
+ * any stream capture.  Every call on a device uses the same array and
+ * leaves its contents behind: calls whose work may overlap on the GPU
+ * (different streams, or different host threads) race on it, so issue
+ * them in one stream order.  lce_check_status() is not available for this
+ * entry point's device status; errors it finds on the device are not
+ * reported. */
+#define LCE_STATIC_SCRATCH_BYTES (32u << 20)
+LCE_API lce_status_t lce_forward_static_ws(int64_t N, int64_t H, int64_t V,
+                                   const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
+                                   const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
+                                   float* loss, float* lse, int64_t* n_valid,
+                                   lce_stream_t stream);
+
 /* Per-kernel device time, for benchmarks.  Between lce_profile_begin() and
  * lce_profile_end(), every kernel the library enqueues is bracketed by two
  * CUDA events recorded on the call's own stream (events are created on

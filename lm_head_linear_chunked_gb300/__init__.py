@@ -23,7 +23,7 @@ __all__ = [
     "LCEError", "IGNORE_INDEX", "WS_FORWARD", "WS_BACKWARD", "WS_FUSED", "STATUS", "library_path", "lib",
     "lce_workspace_size", "lce_chunk_rows", "lce_forward", "lce_backward", "lce_fused_fwd_bwd",
     "lce_check_status", "lce_status_string", "lce_debug_gemm", "lce_debug_wait_timeout",
-    "lce_profile_begin", "lce_profile_end", "PROFILE_KINDS",
+    "lce_profile_begin", "lce_profile_end", "PROFILE_KINDS", "lce_forward_static_ws", "STATIC_SCRATCH_BYTES",
     "workspace", "forward", "backward", "fused",
 ]
 
@@ -55,6 +55,7 @@ _SIGS = {
     "lce_status_string": [_STATUS],
     "lce_debug_gemm": [ctypes.c_int, _I64, _I64, _I64, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "lce_debug_wait_timeout": [ctypes.c_uint32, _P, ctypes.c_size_t, _P],
+    "lce_forward_static_ws": [_I64, _I64, _I64, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _P],
     "lce_profile_begin": [],
     "lce_profile_end": [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64)],
 }
@@ -147,6 +148,17 @@ def lce_fused_fwd_bwd(N, H, V, X, W, b, y, ignore_index, chunk_rows, grad_scale,
                                    _ptr(grad_X), _ptr(grad_W), _ptr(grad_b), _ptr(grad_W_acc), _ptr(grad_b_acc),
                                    _ptr(ws), ws_bytes, _stream(stream)),
            "lce_fused_fwd_bwd")
+
+
+STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def lce_forward_static_ws(N, H, V, X, W, b, y, ignore_index, chunk_rows, loss, lse, n_valid, stream) -> None:
+    """lce_forward with the library's fixed device scratch array instead of a
+    workspace argument, for callers that cannot allocate device memory."""
+    _check(lib().lce_forward_static_ws(N, H, V, _ptr(X), _ptr(W), _ptr(b), _ptr(y), ignore_index, chunk_rows,
+                                       _ptr(loss), _ptr(lse), _ptr(n_valid), _stream(stream)),
+           "lce_forward_static_ws")
 
 
 def lce_check_status(ws, stream) -> int:
