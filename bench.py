@@ -350,7 +350,7 @@ def run_ours(args, w):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "N": N, "H": H, "V": V, "chunk_rows": C, "chunks": n_chunks,
                    "bias": False, "ignored_rows": int((yh == -100).sum().item()),
-                   "l2": "inputs larger than L2 (X 1.07 GB, W 1.24 GB; L2 129 MB)",
+                   "l2": f"inputs larger than L2 (X {N * H * 2 / 1e9:.2f} GB, W {V * H * 2 / 1e9:.2f} GB; L2 129 MB)",
                    "parallelism": "replicas" if ws_n > 1 else "single GPU"},
         "tflops": tflops,
         "flops_per_step": flops,
@@ -384,6 +384,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--shape", default=None,
+                    help="N,H,V: a custom shape with the same input recipe (for profiling small cases)")
     ap.add_argument("--chunk-rows", type=int, default=None)
     ap.add_argument("--cpu-rows", type=int, default=256, help="rows of the CPU-oracle baseline sample")
     ap.add_argument("--ref-rows", type=int, default=32, help="rows per step of --impl reference")
@@ -394,6 +396,9 @@ def main():
         ap.error("--warmup must be at least 3")
     import lce_inputs as L
     w = L.BY_NAME[args.workload]
+    if args.shape:
+        n, h, v = (int(x) for x in args.shape.split(","))
+        w = L.Workload(f"custom-N{n}-H{h}-V{v}", n, 1, h, v, None, "random", 0.05, 0, 7)
     if args.impl == "reference":
         run_reference(args, w)
     else:
