@@ -387,6 +387,35 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def run_gemm(args):
+    """Times the library's bare tensor-core GEMM (lce_debug_gemm) on one shape."""
+    import torch
+
+    import __graft_entry__
+    import lm_head_linear_chunked_gb300 as lce
+    __graft_entry__.build()
+    M, N, K, layout = (int(x) for x in args.gemm.split(","))
+    torch.manual_seed(0)
+    a_shape = (M, K) if layout in (0, 1) else (K, M)
+    b_shape = (N, K) if layout == 0 else (K, N)
+    A = torch.randn(a_shape, device="cuda").to(torch.bfloat16)
+    B = torch.randn(b_shape, device="cuda").to(torch.bfloat16)
+    D = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        lce.lce_debug_gemm(layout, M, N, K, A, B, D, ws, ws.numel(), s)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(args.steps):
+        lce.lce_debug_gemm(layout, M, N, K, A, B, D, ws, ws.numel(), s)
+    e1.record(s)
+    torch.cuda.synchronize()
+    assert lce.lce_check_status(ws, s) == 0
+    t = e0.elapsed_time(e1) / 1e3 / args.steps
+    print(json.dumps({"gemm": [M, N, K, layout], "ms": 1e3 * t, "tflops": 2.0 * M * N * K / t / 1e12}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -399,6 +428,7 @@ def main():
     ap.add_argument("--chunk-rows", type=int, default=None)
     ap.add_argument("--cpu-rows", type=int, default=256, help="rows of the CPU-oracle baseline sample")
     ap.add_argument("--ref-rows", type=int, default=32, help="rows per step of --impl reference")
+    ap.add_argument("--gemm", default=None, help="M,N,K,layout: time the bare GEMM core instead")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -409,7 +439,9 @@ def main():
     if args.shape:
         n, h, v = (int(x) for x in args.shape.split(","))
         w = L.Workload(f"custom-N{n}-H{h}-V{v}", n, 1, h, v, None, "random", 0.05, 0, 7)
-    if args.impl == "reference":
+    if args.gemm:
+        run_gemm(args)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_ours(args, w)

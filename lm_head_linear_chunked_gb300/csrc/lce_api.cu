@@ -13,6 +13,11 @@ namespace lce {
 namespace {
 
 constexpr int64_t AUTO_CHUNK_ROWS = 8192;
+// Tile-order groups: 32 row tiles of X (4096 rows, 32 MB at H = 4096) for
+// the logits passes; 8 column tiles of the fp16 X chunk (2048 columns,
+// 32 MB at 8192 rows) for the grad_W pass.
+constexpr int32_t LOGITS_GROUP_M = 32;
+constexpr int32_t GRADW_GROUP_N = 8;
 constexpr size_t HEADER_BYTES = 1024;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -21,7 +26,8 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 struct Plan {
     int64_t N, H, V, C, n_chunks, n_vt, ldg, mt_chunk, label_blocks_per_chunk;
     bool has_bias;
-    size_t off_row_loss, off_zt, off_pm, off_ps, off_g, off_gb, off_keys, off_counts, off_w16, off_x16, total;
+    size_t off_row_loss, off_zt, off_pm, off_ps, off_g, off_gb, off_keys, off_runs, off_nrun, off_counts, off_w16,
+        off_x16, total;
 };
 
 lce_status_t check_sizes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows) {
@@ -65,6 +71,8 @@ lce_status_t make_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, bool
     p->off_g = take(bwd, static_cast<size_t>(p->C) * p->ldg * 2);
     p->off_gb = take(bwd && has_bias, static_cast<size_t>(p->mt_chunk) * 4 * V * 4);
     p->off_keys = take(bwd, static_cast<size_t>(p->n_chunks) * p->label_blocks_per_chunk * LABEL_BLOCK * 8);
+    p->off_runs = take(bwd, static_cast<size_t>(p->n_chunks) * p->label_blocks_per_chunk * LABEL_BLOCK * 8);
+    p->off_nrun = take(bwd, static_cast<size_t>(p->n_chunks) * p->label_blocks_per_chunk * 4);
     p->off_counts = take(bwd && has_bias, static_cast<size_t>(V) * 4);
     p->off_w16 = take(bwd, static_cast<size_t>(V) * H * 2);
     p->off_x16 = take(bwd, static_cast<size_t>(p->C) * H * 2);
@@ -131,6 +139,7 @@ GemmArgs base_args(WsHeader* hdr) {
     GemmArgs a;
     memset(&a, 0, sizeof(a));
     a.group_m = 1;
+    a.group_n = 1;
     a.status = &hdr->status;
     a.timeout_ns = WAIT_LIMIT_NS;
     return a;
@@ -240,6 +249,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     uint16_t* G = do_bwd ? reinterpret_cast<uint16_t*>(wsb + p.off_g) : nullptr;
     float* gb = (do_bwd && pb.b) ? reinterpret_cast<float*>(wsb + p.off_gb) : nullptr;
     unsigned long long* keys = do_bwd ? reinterpret_cast<unsigned long long*>(wsb + p.off_keys) : nullptr;
+    unsigned long long* runs = do_bwd ? reinterpret_cast<unsigned long long*>(wsb + p.off_runs) : nullptr;
+    int* nrun = do_bwd ? reinterpret_cast<int*>(wsb + p.off_nrun) : nullptr;
     uint16_t* W16 = do_bwd ? reinterpret_cast<uint16_t*>(wsb + p.off_w16) : nullptr;
     uint16_t* X16 = do_bwd ? reinterpret_cast<uint16_t*>(wsb + p.off_x16) : nullptr;
     int* counts = (do_bwd && pb.b) ? reinterpret_cast<int*>(wsb + p.off_counts) : nullptr;
@@ -256,7 +267,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     if (do_bwd) {
         LCE_LAUNCH(PK_OTHER, launch_scale(hdr, o.grad_scale, o.d_grad_output, nullptr, s));
         LCE_LAUNCH(PK_OTHER, launch_label_sort(pb.y, pb.N, p.C, p.label_blocks_per_chunk,
-                                       p.n_chunks * p.label_blocks_per_chunk, pb.V, pb.ignore_index, keys, s));
+                                       p.n_chunks * p.label_blocks_per_chunk, pb.V, pb.ignore_index, keys, runs,
+                                       nrun, s));
         // fp16 operands of the gradient GEMMs, with exact power-of-two scales
         LCE_LAUNCH(PK_OTHER, launch_amax(pb.X, pb.N * pb.H, &hdr->amax_x_bits, s));
         LCE_LAUNCH(PK_OTHER, launch_amax(pb.W, pb.V * pb.H, &hdr->amax_w_bits, s));
@@ -272,7 +284,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             a.m_tiles = static_cast<int32_t>(mt);
             a.n_tiles = static_cast<int32_t>(p.n_vt);
             a.k_blocks = static_cast<int32_t>(cdiv(pb.H, BK));
-            a.raster = 0;
+            a.raster = 2;
+            a.group_m = LOGITS_GROUP_M;
             a.a_y0 = static_cast<int32_t>(r0);
             a.M = rows;
             a.N = pb.V;
@@ -294,7 +307,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.m_tiles = static_cast<int32_t>(mt);
                 a.n_tiles = static_cast<int32_t>(p.n_vt);
                 a.k_blocks = static_cast<int32_t>(cdiv(pb.H, BK));
-                a.raster = 0;
+                a.raster = 2;
+                a.group_m = LOGITS_GROUP_M;
                 a.a_y0 = static_cast<int32_t>(r0);
                 a.M = rows;
                 a.N = pb.V;
@@ -341,7 +355,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.m_tiles = static_cast<int32_t>(cdiv(pb.V, BM));
                 a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
                 a.k_blocks = static_cast<int32_t>(cdiv(rows, BK));
-                a.raster = 1;
+                a.raster = 3;
+                a.group_n = GRADW_GROUP_N;
                 a.M = pb.V;
                 a.N = pb.H;
                 a.scale = &hdr->scale;
@@ -356,11 +371,11 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             }
             // grad_W_acc[y_i] -= s X[i] for the chunk's valid rows, exactly, in row order
             for (int64_t k = 0; k < p.label_blocks_per_chunk; ++k) {
-                const int64_t n = rows - k * LABEL_BLOCK;
-                if (n <= 0) break;
-                LCE_LAUNCH(PK_OTHER, launch_onehot_scatter(keys + (c * p.label_blocks_per_chunk + k) * LABEL_BLOCK,
-                                                   n < LABEL_BLOCK ? n : LABEL_BLOCK, pb.X + r0 * pb.H, pb.H, hdr,
-                                                   o.grad_W_acc, o.grad_W, last && o.grad_W != nullptr, s));
+                if (rows - k * LABEL_BLOCK <= 0) break;
+                const int64_t blk = c * p.label_blocks_per_chunk + k;
+                LCE_LAUNCH(PK_OTHER, launch_onehot_scatter(keys + blk * LABEL_BLOCK, runs + blk * LABEL_BLOCK,
+                                                           nrun + blk, pb.X + r0 * pb.H, pb.H, hdr, o.grad_W_acc,
+                                                           o.grad_W, last && o.grad_W != nullptr, 4 * sm_count(), s));
             }
         }
     }

@@ -57,18 +57,44 @@ __global__ void scale_kernel(WsHeader* hdr, float grad_scale, const float* d_gra
     if (n_valid_out) *n_valid_out = static_cast<int64_t>(nv);
 }
 
-// lse_i = (M + log2 sum_t s_t 2^(m_t - M)) ln 2 over the vocabulary tiles t,
-// in tile order; row loss = lse_i - z[i, y_i] for valid rows, else 0.
-__global__ void combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps, int64_t n_vt,
-                               int64_t ldp, int64_t rows, const float* __restrict__ zt,
-                               const int64_t* __restrict__ y, int64_t ignore_index,
-                               float* __restrict__ lse, float* __restrict__ row_loss) {
-    const int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    if (r >= rows) return;
-    float M = -INFINITY;
-    for (int64_t t = 0; t < n_vt; ++t) M = fmaxf(M, pm[t * ldp + r]);
-    float S = 0.f;
-    for (int64_t t = 0; t < n_vt; ++t) S += ps[t * ldp + r] * exp2f(pm[t * ldp + r] - M);
+// lse_i = (M + log2 S) ln 2, where (M, S) merges the vocabulary tiles'
+// partial (max, sum of 2^(t - max)).  Four threads per row each merge every
+// fourth tile in tile order (S <- S 2^(M - M') + s_t 2^(m_t - M') when a
+// larger max m_t = M' arrives, else S <- S + s_t 2^(m_t - M)); the four
+// results are then merged in a fixed order.  Row loss = lse_i - z[i, y_i]
+// for valid rows, else 0.
+__device__ __forceinline__ void merge_partial(float& M, float& S, float m, float s) {
+    if (m > M) {
+        S = S * exp2f(M - m) + s;
+        M = m;
+    } else if (m > -INFINITY) {
+        S += s * exp2f(m - M);
+    }
+}
+
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
+                                                      int64_t n_vt, int64_t ldp, int64_t rows,
+                                                      const float* __restrict__ zt, const int64_t* __restrict__ y,
+                                                      int64_t ignore_index, float* __restrict__ lse,
+                                                      float* __restrict__ row_loss) {
+    const int g = threadIdx.x & 3;
+    const int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x / 4) + (threadIdx.x >> 2);
+    const bool ok = r < rows;
+    float M = -INFINITY, S = 0.f;
+    if (ok)
+        for (int64_t t = g; t < n_vt; t += 4) merge_partial(M, S, pm[t * ldp + r], ps[t * ldp + r]);
+    // merge the four groups in a fixed order: (g0 with g1), (g2 with g3), then the two pairs
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+        const float M2 = __shfl_xor_sync(0xFFFFFFFFu, M, o);
+        const float S2 = __shfl_xor_sync(0xFFFFFFFFu, S, o);
+        const bool lower = (g & o) == 0;  // both partners merge (lower, upper)
+        float Ma = lower ? M : M2, Sa = lower ? S : S2;
+        merge_partial(Ma, Sa, lower ? M2 : M, lower ? S2 : S);
+        M = Ma;
+        S = Sa;
+    }
+    if (!ok || g != 0) return;
     const float l = (M + log2f(S)) * LN2_F;
     lse[r] = l;
     if (row_loss) row_loss[r] = (y[r] != ignore_index) ? l - zt[r] : 0.f;
@@ -118,10 +144,15 @@ __global__ void grad_b_kernel(const float* __restrict__ gb_part, int64_t parts, 
 // a bitonic network in shared memory.  Ignored rows and out-of-range labels
 // get the largest key and end up last.  Key = label << 32 | row-in-chunk,
 // so rows of one label stay in row order.
+// It also lists the block's runs of equal labels, as (start | end << 32)
+// positions in the sorted order, in no particular order, and their count.
 __global__ void __launch_bounds__(1024) label_sort_kernel(const int64_t* __restrict__ y, int64_t N, int64_t C,
                                                           int64_t blocks_per_chunk, int64_t V,
                                                           int64_t ignore_index,
-                                                          unsigned long long* __restrict__ keys_out) {
+                                                          unsigned long long* __restrict__ keys_out,
+                                                          unsigned long long* __restrict__ runs_out,
+                                                          int* __restrict__ run_count) {
+    __shared__ int nrun;
     extern __shared__ unsigned long long sk[];
     const int64_t b = blockIdx.x;
     const int64_t chunk_start = (b / blocks_per_chunk) * C;
@@ -156,64 +187,117 @@ __global__ void __launch_bounds__(1024) label_sort_kernel(const int64_t* __restr
         }
     }
     for (int i = threadIdx.x; i < LABEL_BLOCK; i += blockDim.x) keys_out[b * LABEL_BLOCK + i] = sk[i];
+    if (threadIdx.x == 0) nrun = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < LABEL_BLOCK; i += blockDim.x) {
+        const unsigned long long k = sk[i];
+        if (k == ~0ull) continue;
+        const unsigned long long v = k >> 32;
+        if (i > 0 && (sk[i - 1] >> 32) == v) continue;
+        int lo = i + 1, hi = LABEL_BLOCK;  // first position past the run (invalid keys never match v)
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((sk[mid] >> 32) == v)
+                lo = mid + 1;
+            else
+                hi = mid;
+        }
+        const int slot = atomicAdd(&nrun, 1);
+        runs_out[b * LABEL_BLOCK + slot] =
+            static_cast<unsigned long long>(i) | (static_cast<unsigned long long>(lo) << 32);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) run_count[b] = nrun;
 }
+
 
 // The one-hot part of grad_W for one sorted block of a chunk:
 //   grad_W_acc[v, :] -= s * sum over the block's rows i with y_i = v of X[i, :]
-// One CTA per run of equal labels (a CTA whose key does not start a run
-// exits), summing the run's rows in row order in fp32, so the result is the
-// same on every call.  Runs have distinct labels, so no two CTAs touch the
-// same grad_W row.  With write_bf16 the updated rows' bf16 cast is rewritten.
-__global__ void __launch_bounds__(256) onehot_scatter_kernel(const unsigned long long* __restrict__ keys, int64_t n,
+// Work items are (run of equal labels, 512-column slab).  Within an item,
+// 64 threads own 8 columns each and four row groups take every fourth row
+// of the run in row order; the four partial sums are added in a fixed
+// order, so the result is the same on every call.  Runs have distinct
+// labels, so no two items touch the same grad_W elements.  With write_bf16
+// the updated elements' bf16 cast is rewritten too.
+__device__ __forceinline__ void add_bf16x8(float (&sum)[8], const uint4 w) {
+    const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        sum[2 * k] += __uint_as_float(q[k] << 16);
+        sum[2 * k + 1] += __uint_as_float(q[k] & 0xFFFF0000u);
+    }
+}
+
+__global__ void __launch_bounds__(256) onehot_scatter_kernel(const unsigned long long* __restrict__ keys,
+                                                             const unsigned long long* __restrict__ runs,
+                                                             const int* __restrict__ run_count,
                                                              const uint16_t* __restrict__ X_chunk, int64_t H,
                                                              const WsHeader* hdr, float* grad_W_acc,
                                                              uint16_t* grad_W, int write_bf16) {
-    const int64_t p = blockIdx.x;
-    if (p >= n) return;
-    const unsigned long long key = keys[p];
-    if (key == ~0ull) return;
-    const unsigned long long v = key >> 32;
-    if (p > 0 && (keys[p - 1] >> 32) == v) return;
-    int64_t q = p + 1;
-    while (q < n && keys[q] != ~0ull && (keys[q] >> 32) == v) ++q;
+    __shared__ float part[3][64][9];
+    const int ct = threadIdx.x & 63, rg = threadIdx.x >> 6;
+    const int slabs = static_cast<int>((H + 511) / 512);
+    const int items = *run_count * slabs;
     const float s = hdr->scale;
-    for (int64_t h = static_cast<int64_t>(threadIdx.x) * 8; h < H; h += static_cast<int64_t>(blockDim.x) * 8) {
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+        const unsigned long long run = runs[item / slabs];
+        const int64_t start = static_cast<int64_t>(run & 0xFFFFFFFFull), end = static_cast<int64_t>(run >> 32);
+        const unsigned long long v = keys[start] >> 32;
+        const int64_t h = static_cast<int64_t>(item % slabs) * 512 + ct * 8;
+        const bool active = h < H;
         float sum[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) sum[k] = 0.f;
-        for (int64_t j = p; j < q; ++j) {
-            const int64_t row = static_cast<int64_t>(keys[j] & 0xFFFFFFFFull);
-            const uint4 w = *reinterpret_cast<const uint4*>(X_chunk + row * H + h);
-            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+        if (active) {
+            int64_t j = start + rg;
+            for (; j + 12 < end; j += 16) {  // four rows of this group in flight
+                uint4 w[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                sum[2 * k] += __uint_as_float(u[k] << 16);
-                sum[2 * k + 1] += __uint_as_float(u[k] & 0xFFFF0000u);
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t row = static_cast<int64_t>(keys[j + 4 * u] & 0xFFFFFFFFull);
+                    w[u] = *reinterpret_cast<const uint4*>(X_chunk + row * H + h);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) add_bf16x8(sum, w[u]);
+            }
+            for (; j < end; j += 4) {
+                const int64_t row = static_cast<int64_t>(keys[j] & 0xFFFFFFFFull);
+                add_bf16x8(sum, *reinterpret_cast<const uint4*>(X_chunk + row * H + h));
             }
         }
-        float* acc = grad_W_acc + static_cast<int64_t>(v) * H + h;
-        float4 a0 = *reinterpret_cast<float4*>(acc);
-        float4 a1 = *reinterpret_cast<float4*>(acc + 4);
-        a0.x = fmaf(-s, sum[0], a0.x);
-        a0.y = fmaf(-s, sum[1], a0.y);
-        a0.z = fmaf(-s, sum[2], a0.z);
-        a0.w = fmaf(-s, sum[3], a0.w);
-        a1.x = fmaf(-s, sum[4], a1.x);
-        a1.y = fmaf(-s, sum[5], a1.y);
-        a1.z = fmaf(-s, sum[6], a1.z);
-        a1.w = fmaf(-s, sum[7], a1.w);
-        *reinterpret_cast<float4*>(acc) = a0;
-        *reinterpret_cast<float4*>(acc + 4) = a1;
-        if (write_bf16) {
-            __nv_bfloat162 b0 = __floats2bfloat162_rn(a0.x, a0.y), b1 = __floats2bfloat162_rn(a0.z, a0.w);
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(a1.x, a1.y), b3 = __floats2bfloat162_rn(a1.z, a1.w);
-            uint4 o;
-            o.x = *reinterpret_cast<uint32_t*>(&b0);
-            o.y = *reinterpret_cast<uint32_t*>(&b1);
-            o.z = *reinterpret_cast<uint32_t*>(&b2);
-            o.w = *reinterpret_cast<uint32_t*>(&b3);
-            *reinterpret_cast<uint4*>(grad_W + static_cast<int64_t>(v) * H + h) = o;
+        if (rg > 0) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) part[rg - 1][ct][k] = sum[k];
         }
+        __syncthreads();
+        if (rg == 0 && active) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sum[k] = ((sum[k] + part[0][ct][k]) + part[1][ct][k]) + part[2][ct][k];
+            float* acc = grad_W_acc + static_cast<int64_t>(v) * H + h;
+            float4 a0 = *reinterpret_cast<float4*>(acc);
+            float4 a1 = *reinterpret_cast<float4*>(acc + 4);
+            a0.x = fmaf(-s, sum[0], a0.x);
+            a0.y = fmaf(-s, sum[1], a0.y);
+            a0.z = fmaf(-s, sum[2], a0.z);
+            a0.w = fmaf(-s, sum[3], a0.w);
+            a1.x = fmaf(-s, sum[4], a1.x);
+            a1.y = fmaf(-s, sum[5], a1.y);
+            a1.z = fmaf(-s, sum[6], a1.z);
+            a1.w = fmaf(-s, sum[7], a1.w);
+            *reinterpret_cast<float4*>(acc) = a0;
+            *reinterpret_cast<float4*>(acc + 4) = a1;
+            if (write_bf16) {
+                __nv_bfloat162 b0 = __floats2bfloat162_rn(a0.x, a0.y), b1 = __floats2bfloat162_rn(a0.z, a0.w);
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(a1.x, a1.y), b3 = __floats2bfloat162_rn(a1.z, a1.w);
+                uint4 o;
+                o.x = *reinterpret_cast<uint32_t*>(&b0);
+                o.y = *reinterpret_cast<uint32_t*>(&b1);
+                o.z = *reinterpret_cast<uint32_t*>(&b2);
+                o.w = *reinterpret_cast<uint32_t*>(&b3);
+                *reinterpret_cast<uint4*>(grad_W + static_cast<int64_t>(v) * H + h) = o;
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -296,7 +380,8 @@ cudaError_t launch_prepass(const int64_t* y, int64_t N, int64_t V, int64_t ignor
 }
 
 cudaError_t launch_label_sort(const int64_t* y, int64_t N, int64_t C, int64_t blocks_per_chunk, int64_t n_blocks,
-                              int64_t V, int64_t ignore_index, unsigned long long* keys, cudaStream_t s) {
+                              int64_t V, int64_t ignore_index, unsigned long long* keys, unsigned long long* runs,
+                              int* run_count, cudaStream_t s) {
     static int configured_device = -1;
     constexpr int smem = LABEL_BLOCK * 8;
     int dev = 0;
@@ -308,16 +393,15 @@ cudaError_t launch_label_sort(const int64_t* y, int64_t N, int64_t C, int64_t bl
         configured_device = dev;
     }
     label_sort_kernel<<<static_cast<unsigned>(n_blocks), 1024, smem, s>>>(y, N, C, blocks_per_chunk, V,
-                                                                          ignore_index, keys);
+                                                                          ignore_index, keys, runs, run_count);
     return cudaGetLastError();
 }
 
-cudaError_t launch_onehot_scatter(const unsigned long long* keys, int64_t n, const uint16_t* X_chunk, int64_t H,
-                                  const WsHeader* hdr, float* grad_W_acc, uint16_t* grad_W, int write_bf16,
-                                  cudaStream_t s) {
-    if (n <= 0) return cudaSuccess;
-    onehot_scatter_kernel<<<static_cast<unsigned>(n), 256, 0, s>>>(keys, n, X_chunk, H, hdr, grad_W_acc, grad_W,
-                                                                   write_bf16);
+cudaError_t launch_onehot_scatter(const unsigned long long* keys, const unsigned long long* runs, const int* run_count,
+                                  const uint16_t* X_chunk, int64_t H, const WsHeader* hdr, float* grad_W_acc,
+                                  uint16_t* grad_W, int write_bf16, int grid, cudaStream_t s) {
+    onehot_scatter_kernel<<<grid, 256, 0, s>>>(keys, runs, run_count, X_chunk, H, hdr, grad_W_acc, grad_W,
+                                               write_bf16);
     return cudaGetLastError();
 }
 
@@ -330,8 +414,8 @@ cudaError_t launch_scale(WsHeader* hdr, float grad_scale, const float* d_grad_ou
 cudaError_t launch_combine(const float* part_m, const float* part_s, int64_t n_vt, int64_t ldp, int64_t rows,
                            const float* zt, const int64_t* y, int64_t ignore_index, float* lse, float* row_loss,
                            cudaStream_t s) {
-    const int threads = 128;
-    const int64_t blocks = (rows + threads - 1) / threads;
+    const int threads = 256;  // 64 rows per block, 4 threads per row
+    const int64_t blocks = (rows + 63) / 64;
     combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(part_m, part_s, n_vt, ldp, rows, zt, y,
                                                                       ignore_index, lse, row_loss);
     return cudaGetLastError();

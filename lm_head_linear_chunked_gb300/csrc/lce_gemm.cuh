@@ -74,7 +74,7 @@ __device__ __forceinline__ void tile_coords(int t, const GemmArgs& a, int& m, in
     } else if (a.raster == 1) {
         n = t % a.n_tiles;
         m = t / a.n_tiles;
-    } else {
+    } else if (a.raster == 2) {  // groups of group_m m-tiles; m fastest within a group
         const int per = a.group_m * a.n_tiles;
         const int g = t / per;
         const int r = t - g * per;
@@ -82,6 +82,14 @@ __device__ __forceinline__ void tile_coords(int t, const GemmArgs& a, int& m, in
         const int gm = min(a.group_m, a.m_tiles - gm0);
         m = gm0 + r % gm;
         n = r / gm;
+    } else {  // groups of group_n n-tiles; n fastest within a group
+        const int per = a.group_n * a.m_tiles;
+        const int g = t / per;
+        const int r = t - g * per;
+        const int gn0 = g * a.group_n;
+        const int gn = min(a.group_n, a.n_tiles - gn0);
+        n = gn0 + r % gn;
+        m = r / gn;
     }
 }
 

@@ -76,8 +76,13 @@ __host__ __device__ inline int operand_scale_exp(unsigned amax_bits) {
 
 struct GemmArgs {
     int32_t m_tiles, n_tiles, k_blocks;
-    int32_t raster;   // 0: m fastest, 1: n fastest, 2: groups of group_m m-tiles
+    // Tile order.  0: m fastest; 1: n fastest; 2: groups of group_m m-tiles
+    // (m fastest inside); 3: groups of group_n n-tiles (n fastest inside).
+    // Groups keep the operand that all tiles of a wave share within about
+    // 32 MB, which L2 holds across waves (64 MB is re-read from DRAM).
+    int32_t raster;
     int32_t group_m;
+    int32_t group_n;
     int32_t a_y0;     // added to A's outer (row) TMA coordinate
     int32_t b_y0;     // added to B's outer (row) TMA coordinate
     int64_t M, N;     // valid extent of the output (rows, columns)
@@ -127,10 +132,12 @@ cudaError_t launch_prepass(const int64_t* y, int64_t N, int64_t V, int64_t ignor
                            WsHeader* hdr, int* label_counts, cudaStream_t s);
 cudaError_t launch_label_sort(const int64_t* y, int64_t N, int64_t C, int64_t blocks_per_chunk,
                               int64_t n_blocks, int64_t V, int64_t ignore_index,
-                              unsigned long long* keys, cudaStream_t s);
-cudaError_t launch_onehot_scatter(const unsigned long long* keys, int64_t n, const uint16_t* X_chunk,
-                                  int64_t H, const WsHeader* hdr, float* grad_W_acc,
-                                  uint16_t* grad_W, int write_bf16, cudaStream_t s);
+                              unsigned long long* keys, unsigned long long* runs, int* run_count,
+                              cudaStream_t s);
+cudaError_t launch_onehot_scatter(const unsigned long long* keys, const unsigned long long* runs,
+                                  const int* run_count, const uint16_t* X_chunk, int64_t H,
+                                  const WsHeader* hdr, float* grad_W_acc, uint16_t* grad_W,
+                                  int write_bf16, int grid, cudaStream_t s);
 cudaError_t launch_scale(WsHeader* hdr, float grad_scale, const float* d_grad_output,
                          int64_t* n_valid_out, cudaStream_t s);
 cudaError_t launch_combine(const float* part_m, const float* part_s, int64_t n_vt, int64_t ldp,

@@ -237,3 +237,16 @@ def test_repeatable_bits():
     c = run_fused(X, W, b, y, 128)
     for k in ("loss", "lse", "grad_X", "grad_W", "grad_W_acc", "grad_b", "grad_b_acc"):
         assert bool((a[k].view(-1) == c[k].view(-1)).all().item()) or k == "loss" and a[k].item() == c[k].item(), k
+
+
+def test_chunk_spanning_several_label_blocks():
+    """A chunk of more than 8192 rows is sorted and scattered in several
+    label blocks; the labels repeat across blocks (Zipf), so the blocks'
+    one-hot updates of the same grad_W rows must all land."""
+    X, W, b, y = random_problem(13, 20000, 64, 512, bias=True)
+    ref = oracle_of(X, W, b, y)
+    bound = fp16_acc_bound(X, W, b, y, ref["lse"], 1.0 / ref["n_valid"])
+    for chunk in (20000, 9000):
+        out = run_fused(X, W, b, y, chunk)
+        assert out["status"] == 0
+        check_against_oracle(out, ref, has_bias=True, acc_bound=bound)
