@@ -126,8 +126,11 @@ LCE_API lce_status_t lce_backward(int64_t N, int64_t H, int64_t V,
 
 /* Forward and backward in one call (the saved-gradient design of the
  * chunk-loss plugin): loss, lse, n_valid, and all gradients, with the same
- * rules as lce_forward and lce_backward.  Cost: 8*N*H*V tensor-core FLOPs
- * (forward logits, recomputed logits, grad_X, grad_W). */
+ * rules as lce_forward and lce_backward.  The forward keeps each chunk's
+ * exponentials 2^(z log2 e - tile max) (fp16) in the workspace and rescales
+ * them to the softmax once lse is known, so the logits are not recomputed:
+ * 6*N*H*V tensor-core FLOPs (forward logits, grad_X, grad_W), against the
+ * 8*N*H*V of lce_forward followed by lce_backward. */
 LCE_API lce_status_t lce_fused_fwd_bwd(int64_t N, int64_t H, int64_t V,
                                const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
                                const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
@@ -203,9 +206,10 @@ LCE_API lce_status_t lce_forward_static_ws(int64_t N, int64_t H, int64_t V,
  * first use and kept; no device memory is allocated).  lce_profile_end()
  * waits for those events and writes, for each kind k < LCE_PROFILE_KINDS,
  * the summed milliseconds ms[k] and the number of launches launches[k]:
- *   0 forward logits + logsumexp     1 backward logits -> softmax P
- *   2 grad_X product                 3 grad_W product
- *   4 all other (label checks, combine, conversions, one-hot part, loss)
+ *   0 forward logits + logsumexp     1 recomputed logits -> softmax P
+ *   2 grad_X product                 3 grad_W product                (lce_backward)
+ *   4 all other (label checks, combine, softmax rescale, conversions,
+ *     one-hot part, loss)
  * Process-wide state: not for concurrent use from several threads. */
 #define LCE_PROFILE_KINDS 5
 LCE_API lce_status_t lce_profile_begin(void);

@@ -60,7 +60,7 @@ _SIGS = {
     "lce_profile_end": [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64)],
 }
 
-PROFILE_KINDS = ("logits_lse", "logits_softmax", "grad_x", "grad_w", "other")
+PROFILE_KINDS = ("logits_lse", "recomputed_logits_softmax", "grad_x", "grad_w", "other")
 
 
 class LCEError(RuntimeError):

@@ -296,13 +296,20 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             a.part_s = ps;
             a.zt = zt;
             a.ldp = p.C;
+            if (do_bwd) {  // keep E = 2^(t - tile max) for the backward: no recompute
+                a.g = G;
+                a.ldg = p.ldg;
+            }
             LCE_LAUNCH(PK_LSE, launch_gemm(MODE_LSE, mX_k, mW_k, a, grid_for(mt * p.n_vt), s));
             LCE_LAUNCH(PK_OTHER, launch_combine(pm, ps, p.n_vt, p.C, rows, zt, pb.y + r0, pb.ignore_index, o.lse + r0,
                                         row_loss + r0, s));
         }
         if (do_bwd) {
             const bool first = c == 0, last = c == p.n_chunks - 1;
-            {   // recompute the logits; P = softmax (bf16)
+            if (do_fwd) {  // P = E 2^(tile max - lse), in place
+                LCE_LAUNCH(PK_OTHER, launch_p_rescale(G, p.ldg, rows, pb.V, pm, p.C, o.lse + r0, pb.y + r0,
+                                                      pb.ignore_index, gb, s));
+            } else {   // recompute the logits; P = softmax (fp16)
                 GemmArgs a = base_args(hdr);
                 a.m_tiles = static_cast<int32_t>(mt);
                 a.n_tiles = static_cast<int32_t>(p.n_vt);

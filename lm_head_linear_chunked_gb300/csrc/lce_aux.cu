@@ -100,6 +100,64 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     if (row_loss) row_loss[r] = (y[r] != ignore_index) ? l - zt[r] : 0.f;
 }
 
+// The fused path's softmax without recomputing the logits: the forward
+// stored E = fp16(2^(t - m) 2^15) per (row, 256-column vocab tile) with m the
+// tile's max; here, once lse is known, P = fp16(E 2^(m - lse log2 e)) in
+// place (= fp16(p 2^15)), 0 for ignored rows.  One block covers 32 rows of
+// one vocab tile: 32 threads x 8 columns, 8 rows at a time.  With gb_part,
+// it also writes the block's fp32 column sums of p (row order fixed).
+__global__ void __launch_bounds__(256) p_rescale_kernel(uint16_t* __restrict__ P, int64_t ldg, int64_t rows,
+                                                        int64_t V, const float* __restrict__ pm, int64_t ldp,
+                                                        const float* __restrict__ lse,
+                                                        const int64_t* __restrict__ y, int64_t ignore_index,
+                                                        float* __restrict__ gb_part) {
+    __shared__ float colsum[8][256 + 4];
+    constexpr float LOG2E = 1.4426950408889634f;
+    const int cg = threadIdx.x & 31, rr = threadIdx.x >> 5;
+    const int64_t tile = blockIdx.y;
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * 32;
+    const int64_t c = tile * 256 + cg * 8;
+    const int64_t cend = (tile * 256 + 256 < ldg) ? tile * 256 + 256 : ldg;
+    const bool col_ok = c < cend;
+    float sum[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) sum[k] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int64_t r = row0 + rr + 8 * q;
+        if (r >= rows || !col_ok) continue;
+        const int64_t yr = y[r];
+        const bool valid = yr != ignore_index && yr >= 0 && yr < V;
+        const float f = valid ? exp2f(pm[tile * ldp + r] - lse[r] * LOG2E) : 0.f;
+        uint4* ptr = reinterpret_cast<uint4*>(P + r * ldg + c);
+        const uint4 w = *ptr;
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            __half2 h = *reinterpret_cast<const __half2*>(&u[k]);
+            const float2 e = __half22float2(h);
+            const float p0 = e.x * f, p1 = e.y * f;
+            sum[2 * k] += p0;
+            sum[2 * k + 1] += p1;
+            __half2 out = __floats2half2_rn(p0, p1);
+            o[k] = *reinterpret_cast<uint32_t*>(&out);
+        }
+        *ptr = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (!gb_part) return;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) colsum[rr][cg * 8 + k] = sum[k];
+    __syncthreads();
+    const int64_t v = tile * 256 + threadIdx.x;
+    if (v < V) {
+        float t = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t += colsum[k][threadIdx.x];
+        gb_part[blockIdx.x * V + v] = t * (1.f / static_cast<float>(1 << P_SCALE_EXP));
+    }
+}
+
 // loss = sum of row losses / n_valid.  One block; the summation order
 // depends on N only, so the result does not depend on the chunk size.
 __global__ void loss_kernel(const float* __restrict__ row_loss, int64_t N, const WsHeader* hdr,
@@ -456,6 +514,16 @@ cudaError_t launch_to_f16_scaled(const uint16_t* x, int64_t n, const unsigned* a
     const int64_t want = (n / 8 + threads - 1) / threads;
     const int blocks = static_cast<int>(want < 1 ? 1 : (want < 4096 ? want : 4096));
     to_f16_scaled_kernel<<<blocks, threads, 0, s>>>(x, n, amax_bits, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_p_rescale(uint16_t* P, int64_t ldg, int64_t rows, int64_t V, const float* pm, int64_t ldp,
+                             const float* lse, const int64_t* y, int64_t ignore_index, float* gb_part,
+                             cudaStream_t s) {
+    // every 32-row block of every 128-row tile writes its column sums (zeros
+    // past the last row), the layout the grad_b accumulation reads
+    const dim3 grid(static_cast<unsigned>((rows + 127) / 128 * 4), static_cast<unsigned>((V + 255) / 256));
+    p_rescale_kernel<<<grid, 256, 0, s>>>(P, ldg, rows, V, pm, ldp, lse, y, ignore_index, gb_part);
     return cudaGetLastError();
 }
 

@@ -187,8 +187,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
     const bool row_ok = row < a.M;
 
     if constexpr (MODE == MODE_LSE) {
+        // Two passes over the tile's TMEM row.  Pass 1: the tile max of
+        // t = z log2(e) and the target logit.  Pass 2: s = sum 2^(t - max),
+        // and with a.g set, E = fp16(2^(t - max) * 2^P_SCALE_EXP) for the
+        // backward (rescaled to P once lse is known).
         const int64_t yr = row_ok ? a.y[row] : a.ignore_index;
-        float mx = -INFINITY, sm = 0.f, zt = 0.f;
+        float mx = -INFINITY, zt = 0.f;
         bool got = false;
 #pragma unroll 1
         for (int j = 0; j < BN / 32; ++j) {
@@ -201,20 +205,28 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
             const int64_t d = yr - c0;
             const int kk = (d >= 0 && d < 32) ? static_cast<int>(d) : -1;
             got |= kk >= 0;
-            float cm = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 zt = (i == kk) ? v[i] : zt;
-                const float t = (i < nv) ? v[i] * LOG2E_F : -INFINITY;
-                v[i] = t;
-                cm = fmaxf(cm, t);
+                if (i < nv) mx = fmaxf(mx, v[i] * LOG2E_F);
             }
-            const float mn = fmaxf(mx, cm);
-            float acc = 0.f;
+        }
+        float sm = 0.f;
+#pragma unroll 1
+        for (int j = 0; j < BN / 32; ++j) {
+            const int64_t c0 = col0 + 32 * j;
+            if (c0 >= a.N) break;
+            float v[32];
+            tmem_load_32cols(taddr + 32 * j, v);
+            const int nv = static_cast<int>(min64(32, a.N - c0));
+            if (a.bias) add_bias32(v, a.bias + c0, nv);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc += fast_exp2(v[i] - mn);
-            sm = sm * fast_exp2(mx - mn) + acc;
-            mx = mn;
+            for (int i = 0; i < 32; ++i) {
+                const float e = (i < nv) ? fast_exp2(v[i] * LOG2E_F - mx) : 0.f;
+                sm += e;
+                v[i] = e * P_SCALE;
+            }
+            if (a.g && row_ok) store_f16_32(a.g + row * a.ldg + c0, v, static_cast<int>(min64(32, a.ldg - c0)));
         }
         tc_fence_before_sync();
         __syncwarp();

@@ -16,7 +16,8 @@ enum GemmMode : int {
     MODE_PLAIN_KK = 0,  // D = A B^T,  A [M,K], B [N,K]        (both K-major)
     MODE_PLAIN_KM = 1,  // D = A B,    A [M,K], B [K,N]        (B MN-major)
     MODE_PLAIN_MM = 2,  // D = A^T B,  A [K,M], B [K,N]        (both MN-major)
-    MODE_LSE = 3,       // logits X_c W^T -> per-row partial (max, sum exp), target logit
+    MODE_LSE = 3,       // logits X_c W^T -> per-row partial (max, sum exp), target logit,
+                        //   optionally E = 2^(t - tile max) for the backward
     MODE_G = 4,         // logits X_c W^T -> P = softmax (fp16, scaled by 2^P_SCALE_EXP), bias column sums
     MODE_GRADX = 5,     // grad_X_c = s * (P W - W[y])           (fp16 operands, bf16 out)
     MODE_GRADW = 6,     // grad_W_acc (+)= s * P^T X_c           (fp16 operands, fp32 accumulator, bf16 cast)
@@ -149,6 +150,9 @@ cudaError_t launch_grad_b(const float* gb_part, int64_t parts, int64_t V, const 
                           const int* label_counts, float* grad_b_acc, uint16_t* grad_b, int first,
                           int last, cudaStream_t s);
 cudaError_t launch_wait_probe(unsigned* status, uint64_t limit_ns, cudaStream_t s);
+cudaError_t launch_p_rescale(uint16_t* P, int64_t ldg, int64_t rows, int64_t V, const float* pm, int64_t ldp,
+                             const float* lse, const int64_t* y, int64_t ignore_index, float* gb_part,
+                             cudaStream_t s);
 cudaError_t launch_amax(const uint16_t* x, int64_t n, unsigned* amax_bits, cudaStream_t s);
 cudaError_t launch_to_f16_scaled(const uint16_t* x, int64_t n, const unsigned* amax_bits, uint16_t* out,
                                  cudaStream_t s);
