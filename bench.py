@@ -44,6 +44,12 @@ sys.path.insert(0, ROOT)
 METRIC = "tokens/s fused LCE fwd+bwd (Qwen3-8B head) and % of BF16 tensor peak"
 WORKLOAD = "qwen3-8b-head-N131072-H4096-V151936"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+# DRAM bytes (read + write) of one full-size launch of each GEMM role on this
+# workload, from the ncu capture summarised in
+# profiles/gemm_dram_full_qwen3-8b-head.md.  None once a kernel has changed
+# since its counters were taken.
+DRAM_BYTES_PER_LAUNCH = {"grad_w": 7.75e9 + 2.47e9, "grad_x": 11.70e9 + 0.06e9,
+                         "logits_lse": None, "recomputed_logits_softmax": None}
 
 
 def load_peaks():
@@ -292,44 +298,83 @@ def run_ours(args, w):
         raise RuntimeError(f"device status after timed steps: {lce.STATUS[st]}")
     t_step = max_over_ranks(t_step)
 
-    # ---- end to end: host buffers, copies inside the timed region
+    # ---- end to end: host buffers, copies inside the timed region.  Two sets
+    # of device buffers: step k+1's inputs are copied in while step k
+    # computes, and step k's results are copied out while step k+1 computes.
     e2e = None
     if not args.no_e2e:
-        lse_h = torch.empty(N, dtype=torch.float32, pin_memory=True)
-        loss_h = torch.empty(1, dtype=torch.float32, pin_memory=True)
-        gX_h = torch.empty((N, H), dtype=torch.bfloat16, pin_memory=True)
-        gW_h = torch.empty((V, H), dtype=torch.bfloat16, pin_memory=True)
+        def device_set():
+            return {"X": torch.empty_like(X), "W": torch.empty_like(W), "y": torch.empty_like(y),
+                    "loss": torch.empty_like(loss), "lse": torch.empty_like(lse), "n_valid": torch.empty_like(n_valid),
+                    "gX": torch.empty_like(gX), "gW": torch.empty_like(gW), "gW_acc": torch.empty_like(gW_acc),
+                    "ws": torch.empty_like(ws)}
 
-        def e2e_step():
-            with torch.cuda.stream(s):
-                X.copy_(Xh, non_blocking=True)
-                W.copy_(Wh, non_blocking=True)
-                y.copy_(yh, non_blocking=True)
-                step()
-                loss_h.copy_(loss, non_blocking=True)
-                lse_h.copy_(lse, non_blocking=True)
-                gX_h.copy_(gX, non_blocking=True)
-                gW_h.copy_(gW, non_blocking=True)
+        def host_set():
+            return {"loss": torch.empty(1, dtype=torch.float32, pin_memory=True),
+                    "lse": torch.empty(N, dtype=torch.float32, pin_memory=True),
+                    "gX": torch.empty((N, H), dtype=torch.bfloat16, pin_memory=True),
+                    "gW": torch.empty((V, H), dtype=torch.bfloat16, pin_memory=True)}
 
-        e2e_step()
-        barrier()
+        dsets = [device_set(), device_set()]
+        hsets = [host_set(), host_set()]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+        def run_steps(k_steps, t0=None, t1=None):
+            comp_done, out_done = [], []
+            if t0 is not None:
+                t0.record(s_in)
+            for k in range(k_steps):
+                d, h = dsets[k % 2], hsets[k % 2]
+                if k >= 2:
+                    s_in.wait_event(comp_done[k - 2])       # set's inputs no longer read
+                with torch.cuda.stream(s_in):
+                    d["X"].copy_(Xh, non_blocking=True)
+                    d["W"].copy_(Wh, non_blocking=True)
+                    d["y"].copy_(yh, non_blocking=True)
+                    in_done = torch.cuda.Event()
+                    in_done.record(s_in)
+                s.wait_event(in_done)
+                if k >= 2:
+                    s.wait_event(out_done[k - 2])           # set's results already copied out
+                lce.lce_fused_fwd_bwd(N, H, V, d["X"], d["W"], None, d["y"], -100, chunk, 1.0, None, d["loss"],
+                                      d["lse"], d["n_valid"], d["gX"], d["gW"], None, d["gW_acc"], None, d["ws"],
+                                      nws, s)
+                ev = torch.cuda.Event()
+                ev.record(s)
+                comp_done.append(ev)
+                s_out.wait_event(ev)
+                with torch.cuda.stream(s_out):
+                    h["loss"].copy_(d["loss"], non_blocking=True)
+                    h["lse"].copy_(d["lse"], non_blocking=True)
+                    h["gX"].copy_(d["gX"], non_blocking=True)
+                    h["gW"].copy_(d["gW"], non_blocking=True)
+                    ev2 = torch.cuda.Event()
+                    ev2.record(s_out)
+                out_done.append(ev2)
+            if t1 is not None:
+                t1.record(s_out)
+
+        run_steps(2)
         torch.cuda.synchronize(dev)
+        barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(s)
+        run_steps(args.steps, e0, e1)
         torch.cuda.synchronize(dev)
         barrier()
-        t_e2e = e0.elapsed_time(e1) / 1e3 / args.steps
-        t_e2e = max_over_ranks(t_e2e)
+        for d in dsets:
+            st = lce.lce_check_status(d["ws"], s)
+            if st != 0:
+                raise RuntimeError(f"device status after end-to-end steps: {lce.STATUS[st]}")
+        t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps)
         h2d = Xh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 8
-        d2h = 4 + N * 4 + gX_h.numel() * 2 + gW_h.numel() * 2
+        d2h = 4 + N * 4 + N * H * 2 + V * H * 2
         e2e = {"value": replica_rate(N, ws_n, t_e2e), "unit": "tokens/s", "ms_per_step": 1e3 * t_e2e,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "path": "lce_fused_fwd_bwd via the Python binding, pinned host buffers"}
-        loss_v = float(loss_h.item())
+               "path": "lce_fused_fwd_bwd via the Python binding; inputs copied from pinned host memory and "
+                       "loss, lse, grad_X, grad_W copied back every step, double-buffered so a step's copies "
+                       "overlap its neighbours' compute"}
+        loss_v = float(hsets[(args.steps - 1) % 2]["loss"].item())
     else:
         loss_v = float(loss.item())
 
@@ -372,7 +417,10 @@ def run_ours(args, w):
         "frac_of_peak": {"measured_burst_bf16": tflops / burst, "measured_sustained_bf16": tflops / sustained,
                          "nominal_dense_bf16_2250": tflops / 2250.0, "peak_source": peak_src},
         "roofline": {"bound": "tensor", "achieved": dom_tflops, "peak": sustained, "unit": "TFLOP/s",
-                     "frac": dom_tflops / sustained, "traffic": None, "kernel": f"gemm_kernel ({dom})",
+                     "frac": dom_tflops / sustained,
+                     "traffic": DRAM_BYTES_PER_LAUNCH.get(dom) if args.workload == WORKLOAD and not args.shape
+                     and C == 8192 else None,
+                     "kernel": f"gemm_kernel ({dom})",
                      "flops_per_launch": dom_flops_per_launch, "launches": dom_n,
                      "mean_launch_ms": dom_ms / dom_n,
                      "peak_source": f"{peak_src} sustained bf16 (fp16 operands run at the bf16 rate)"},
