@@ -140,6 +140,20 @@ LCE_API lce_status_t lce_fused_fwd_bwd(int64_t N, int64_t H, int64_t V,
                                float* grad_W_acc, float* grad_b_acc,
                                void* ws, size_t ws_bytes, lce_stream_t stream);
 
+/* The backward of the chunk-loss plugin's saved-gradient design (LlamaFactory
+ * PR #10762 analysis page, section 4: the Function computes the gradients in
+ * its forward, and its backward scales them by grad_output).  After an
+ * lce_fused_fwd_bwd call with grad_scale 1 and no grad_output, with
+ * g = *d_grad_output (a device float):
+ *   grad_X <- bf16(g * grad_X) in place (may be NULL),
+ *   grad_W <- bf16(g * grad_W_acc), grad_b <- bf16(g * grad_b_acc)
+ * (each output and its accumulator both given or both NULL; the fp32
+ * accumulators are not changed).  Device pointers, 16-byte aligned,
+ * H % 8 == 0.  Enqueued on `stream`. */
+LCE_API lce_status_t lce_scale_grads(int64_t N, int64_t H, int64_t V, const float* d_grad_output,
+                             lce_bf16* grad_X, const float* grad_W_acc, lce_bf16* grad_W,
+                             const float* grad_b_acc, lce_bf16* grad_b, lce_stream_t stream);
+
 /* Synchronises `stream`, then returns the device status of the last call
  * that used workspace `ws` (LCE_OK, LCE_ERR_LABEL_RANGE, LCE_ERR_TIMEOUT),
  * or LCE_ERR_CUDA if the stream reported an error. */

@@ -12,12 +12,17 @@
 namespace lce {
 namespace {
 
-constexpr int64_t AUTO_CHUNK_ROWS = 8192;
+constexpr int64_t AUTO_CHUNK_ROWS = 16384;
 // Tile-order groups: 32 row tiles of X (4096 rows, 32 MB at H = 4096) for
-// the logits passes; 8 column tiles of the fp16 X chunk (2048 columns,
-// 32 MB at 8192 rows) for the grad_W pass.
+// the logits passes; for the grad_W pass, as many 256-column tiles of the
+// fp16 X chunk as make about 32 MB (8 at 8192 rows, 4 at 16384).
 constexpr int32_t LOGITS_GROUP_M = 32;
-constexpr int32_t GRADW_GROUP_N = 8;
+constexpr int64_t GROUP_BYTES = 32ll << 20;
+
+int32_t gradw_group_n(int64_t rows) {
+    const int64_t g = GROUP_BYTES / (rows * BN * 2);
+    return static_cast<int32_t>(g < 1 ? 1 : (g > 64 ? 64 : g));
+}
 constexpr size_t HEADER_BYTES = 1024;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -363,7 +368,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
                 a.k_blocks = static_cast<int32_t>(cdiv(rows, BK));
                 a.raster = 3;
-                a.group_n = GRADW_GROUP_N;
+                a.group_n = gradw_group_n(rows);
                 a.M = pb.V;
                 a.N = pb.H;
                 a.scale = &hdr->scale;
@@ -477,6 +482,19 @@ lce_status_t lce_fused_fwd_bwd(int64_t N, int64_t H, int64_t V, const lce_bf16* 
     o.grad_W_acc = grad_W_acc;
     o.grad_b_acc = grad_b_acc;
     return run(pb, o, true, true, chunk_rows, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lce_status_t lce_scale_grads(int64_t N, int64_t H, int64_t V, const float* d_grad_output, lce_bf16* grad_X,
+                             const float* grad_W_acc, lce_bf16* grad_W, const float* grad_b_acc, lce_bf16* grad_b,
+                             lce_stream_t stream) {
+    if (N <= 0 || H <= 0 || V <= 0 || !d_grad_output) return LCE_ERR_INVALID_ARG;
+    if ((grad_W != nullptr) != (grad_W_acc != nullptr) || (grad_b != nullptr) != (grad_b_acc != nullptr))
+        return LCE_ERR_INVALID_ARG;
+    if (!aligned16(grad_X) || !aligned16(grad_W_acc) || !aligned16(grad_W)) return LCE_ERR_INVALID_ARG;
+    if (H % 8 != 0) return LCE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    LCE_LAUNCH(PK_OTHER, launch_scale_grads(N, H, V, d_grad_output, grad_X, grad_W_acc, grad_W, grad_b_acc, grad_b, s));
+    return LCE_OK;
 }
 
 lce_status_t lce_check_status(const void* ws, lce_stream_t stream) {

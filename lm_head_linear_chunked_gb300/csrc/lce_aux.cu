@@ -359,6 +359,43 @@ __global__ void __launch_bounds__(256) onehot_scatter_kernel(const unsigned long
     }
 }
 
+// The backward of the saved-gradient design: g = *d_grad_output;
+// grad_X <- bf16(g grad_X) in place, grad_W <- bf16(g grad_W_acc),
+// grad_b <- bf16(g grad_b_acc) (the fp32 accumulators are left as they are).
+__global__ void scale_grads_kernel(int64_t nx8, int64_t nw8, int64_t V, const float* d_grad_output,
+                                   uint4* __restrict__ grad_X, const float4* __restrict__ grad_W_acc,
+                                   uint4* __restrict__ grad_W, const float* __restrict__ grad_b_acc,
+                                   uint16_t* __restrict__ grad_b) {
+    const float g = *d_grad_output;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t t0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    for (int64_t i = t0; i < nx8; i += stride) {
+        const uint4 w = grad_X[i];
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(g * __uint_as_float(u[k] << 16),
+                                                     g * __uint_as_float(u[k] & 0xFFFF0000u));
+            o[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        grad_X[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (grad_W)
+        for (int64_t i = t0; i < nw8; i += stride) {
+            const float4 a = grad_W_acc[2 * i], b = grad_W_acc[2 * i + 1];
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(g * a.x, g * a.y), h1 = __floats2bfloat162_rn(g * a.z, g * a.w);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(g * b.x, g * b.y), h3 = __floats2bfloat162_rn(g * b.z, g * b.w);
+            grad_W[i] = make_uint4(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
+                                   *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
+        }
+    if (grad_b)
+        for (int64_t v = t0; v < V; v += stride) {
+            __nv_bfloat16 h = __float2bfloat16_rn(g * grad_b_acc[v]);
+            grad_b[v] = *reinterpret_cast<uint16_t*>(&h);
+        }
+}
+
 // max |x| over bf16 values, as float bits (non-negative floats order like
 // their bit patterns, so an integer max is exact and order-independent).
 __global__ void amax_kernel(const uint16_t* __restrict__ x, int64_t n, unsigned* amax_bits) {
@@ -524,6 +561,20 @@ cudaError_t launch_p_rescale(uint16_t* P, int64_t ldg, int64_t rows, int64_t V, 
     // past the last row), the layout the grad_b accumulation reads
     const dim3 grid(static_cast<unsigned>((rows + 127) / 128 * 4), static_cast<unsigned>((V + 255) / 256));
     p_rescale_kernel<<<grid, 256, 0, s>>>(P, ldg, rows, V, pm, ldp, lse, y, ignore_index, gb_part);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale_grads(int64_t N, int64_t H, int64_t V, const float* d_grad_output, uint16_t* grad_X,
+                               const float* grad_W_acc, uint16_t* grad_W, const float* grad_b_acc,
+                               uint16_t* grad_b, cudaStream_t s) {
+    const int64_t nx8 = grad_X ? N * H / 8 : 0, nw8 = grad_W ? V * H / 8 : 0;
+    const int64_t most = nx8 > nw8 ? nx8 : nw8;
+    const int64_t want = (most + 255) / 256;
+    const int blocks = static_cast<int>(want < 1 ? 1 : (want < 8192 ? want : 8192));
+    scale_grads_kernel<<<blocks, 256, 0, s>>>(nx8, nw8, grad_b ? V : 0, d_grad_output,
+                                              reinterpret_cast<uint4*>(grad_X),
+                                              reinterpret_cast<const float4*>(grad_W_acc),
+                                              reinterpret_cast<uint4*>(grad_W), grad_b_acc, grad_b);
     return cudaGetLastError();
 }
 

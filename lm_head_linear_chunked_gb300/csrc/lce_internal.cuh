@@ -153,6 +153,9 @@ cudaError_t launch_wait_probe(unsigned* status, uint64_t limit_ns, cudaStream_t 
 cudaError_t launch_p_rescale(uint16_t* P, int64_t ldg, int64_t rows, int64_t V, const float* pm, int64_t ldp,
                              const float* lse, const int64_t* y, int64_t ignore_index, float* gb_part,
                              cudaStream_t s);
+cudaError_t launch_scale_grads(int64_t N, int64_t H, int64_t V, const float* d_grad_output, uint16_t* grad_X,
+                               const float* grad_W_acc, uint16_t* grad_W, const float* grad_b_acc,
+                               uint16_t* grad_b, cudaStream_t s);
 cudaError_t launch_amax(const uint16_t* x, int64_t n, unsigned* amax_bits, cudaStream_t s);
 cudaError_t launch_to_f16_scaled(const uint16_t* x, int64_t n, const unsigned* amax_bits, uint16_t* out,
                                  cudaStream_t s);

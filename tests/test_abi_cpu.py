@@ -44,8 +44,8 @@ def test_status_strings():
     assert lce.lce_status_string(99) == "unknown status"
 
 
-@pytest.mark.parametrize("N,chunk,expect", [(512, 256, 256), (512, 0, 512), (100000, 0, 8192), (7, 1000, 7),
-                                            (131072, 0, 8192), (4096, 1, 1)])
+@pytest.mark.parametrize("N,chunk,expect", [(512, 256, 256), (512, 0, 512), (100000, 0, 16384), (7, 1000, 7),
+                                            (131072, 0, 16384), (4096, 1, 1)])
 def test_chunk_rows(N, chunk, expect):
     assert lce.lce_chunk_rows(N, 1024, 32768, chunk) == expect
 
@@ -56,8 +56,8 @@ def test_workspace_sizes():
     b = lce.lce_workspace_size(N, H, V, 0, False, lce.WS_BACKWARD)
     fb = lce.lce_workspace_size(N, H, V, 0, False, lce.WS_FUSED)
     assert fb >= max(f, b) and fb <= f + b
-    assert b >= 8192 * V * 2                       # one chunk of bf16 G
-    assert fb < N * V * 2 / 10                     # far below the logits it replaces
+    assert b >= 16384 * V * 2                      # one chunk of fp16 P
+    assert fb < N * V * 2 / 5                      # far below the logits it replaces
     with_bias = lce.lce_workspace_size(N, H, V, 0, True, lce.WS_FUSED)
     assert with_bias > fb
     assert lce.lce_workspace_size(N, H, V, 256, False, lce.WS_FUSED) < fb
