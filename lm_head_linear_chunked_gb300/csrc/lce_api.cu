@@ -32,7 +32,7 @@ struct Plan {
     int64_t N, H, V, C, n_chunks, n_vt, ldg, mt_chunk, label_blocks_per_chunk;
     bool has_bias;
     size_t off_row_loss, off_zt, off_pm, off_ps, off_g, off_gb, off_keys, off_runs, off_nrun, off_counts, off_w16,
-        off_x16, total;
+        off_x16, off_dmap, off_crow, off_nvc, total;
 };
 
 lce_status_t check_sizes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows) {
@@ -81,6 +81,9 @@ lce_status_t make_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, bool
     p->off_counts = take(bwd && has_bias, static_cast<size_t>(V) * 4);
     p->off_w16 = take(bwd, static_cast<size_t>(V) * H * 2);
     p->off_x16 = take(bwd, static_cast<size_t>(p->C) * H * 2);
+    p->off_dmap = take(bwd, static_cast<size_t>(N) * 4);
+    p->off_crow = take(bwd, static_cast<size_t>(N) * 4);
+    p->off_nvc = take(bwd, static_cast<size_t>(p->n_chunks) * 4);
     p->total = off;
     return LCE_OK;
 }
@@ -258,6 +261,9 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     int* nrun = do_bwd ? reinterpret_cast<int*>(wsb + p.off_nrun) : nullptr;
     uint16_t* W16 = do_bwd ? reinterpret_cast<uint16_t*>(wsb + p.off_w16) : nullptr;
     uint16_t* X16 = do_bwd ? reinterpret_cast<uint16_t*>(wsb + p.off_x16) : nullptr;
+    int* dmap = do_bwd ? reinterpret_cast<int*>(wsb + p.off_dmap) : nullptr;  // row -> compacted row or -1
+    int* crow = do_bwd ? reinterpret_cast<int*>(wsb + p.off_crow) : nullptr;  // compacted row -> chunk row
+    int* nvc = do_bwd ? reinterpret_cast<int*>(wsb + p.off_nvc) : nullptr;    // valid rows per chunk
     int* counts = (do_bwd && pb.b) ? reinterpret_cast<int*>(wsb + p.off_counts) : nullptr;
 
     // operand maps of the whole X and W
@@ -278,6 +284,10 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
         LCE_LAUNCH(PK_OTHER, launch_amax(pb.X, pb.N * pb.H, &hdr->amax_x_bits, s));
         LCE_LAUNCH(PK_OTHER, launch_amax(pb.W, pb.V * pb.H, &hdr->amax_w_bits, s));
         LCE_LAUNCH(PK_OTHER, launch_to_f16_scaled(pb.W, pb.V * pb.H, &hdr->amax_w_bits, W16, s));
+        // the backward products run over each chunk's valid rows only
+        LCE_LAUNCH(PK_OTHER, launch_compact_rows(pb.y, pb.N, p.C, p.n_chunks, pb.V, pb.ignore_index, dmap, crow,
+                                                 nvc, s));
+        if (o.grad_X) LCE_LAUNCH(PK_OTHER, launch_zero_ignored_rows(dmap, pb.N, pb.H, o.grad_X, s));
     }
 
     for (int64_t c = 0; c < p.n_chunks; ++c) {
@@ -301,9 +311,10 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             a.part_s = ps;
             a.zt = zt;
             a.ldp = p.C;
-            if (do_bwd) {  // keep E = 2^(t - tile max) for the backward: no recompute
+            if (do_bwd) {  // keep E = 2^(t - tile max) of the valid rows for the backward: no recompute
                 a.g = G;
                 a.ldg = p.ldg;
+                a.row_map = dmap + r0;
             }
             LCE_LAUNCH(PK_LSE, launch_gemm(MODE_LSE, mX_k, mW_k, a, grid_for(mt * p.n_vt), s));
             LCE_LAUNCH(PK_OTHER, launch_combine(pm, ps, p.n_vt, p.C, rows, zt, pb.y + r0, pb.ignore_index, o.lse + r0,
@@ -312,8 +323,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
         if (do_bwd) {
             const bool first = c == 0, last = c == p.n_chunks - 1;
             if (do_fwd) {  // P = E 2^(tile max - lse), in place
-                LCE_LAUNCH(PK_OTHER, launch_p_rescale(G, p.ldg, rows, pb.V, pm, p.C, o.lse + r0, pb.y + r0,
-                                                      pb.ignore_index, gb, s));
+                LCE_LAUNCH(PK_OTHER, launch_p_rescale(G, p.ldg, rows, pb.V, pm, p.C, o.lse + r0, crow + r0, nvc + c,
+                                                      gb, s));
             } else {   // recompute the logits; P = softmax (fp16)
                 GemmArgs a = base_args(hdr);
                 a.m_tiles = static_cast<int32_t>(mt);
@@ -331,12 +342,14 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.g = G;
                 a.ldg = p.ldg;
                 a.gb_part = gb;
+                a.row_map = dmap + r0;
                 LCE_LAUNCH(PK_P, launch_gemm(MODE_G, mX_k, mW_k, a, grid_for(mt * p.n_vt), s));
             }
             if (gb)
                 LCE_LAUNCH(PK_OTHER, launch_grad_b(gb, mt * 4, pb.V, hdr, counts, o.grad_b_acc, o.grad_b, first, last, s));
             // P and X_c maps bounded to this chunk's rows: rows past it read as zero
-            LCE_LAUNCH(PK_OTHER, launch_to_f16_scaled(pb.X + r0 * pb.H, rows * pb.H, &hdr->amax_x_bits, X16, s));
+            LCE_LAUNCH(PK_OTHER, launch_gather_f16(pb.X + r0 * pb.H, pb.H, crow + r0, nvc + c, rows, &hdr->amax_x_bits,
+                                                   X16, do_fwd ? nullptr : G, p.ldg, s));
             CUtensorMap mG_k, mG_mn, mX16_mn;
             if (!map_16bit_2d(&mG_k, G, rows, pb.V, p.ldg, 64, BM, true) ||
                 !map_16bit_2d(&mG_mn, G, rows, pb.V, p.ldg, 64, 64, true) ||
@@ -360,6 +373,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.ldw = pb.H;
                 a.V = pb.V;
                 a.b_amax_bits = &hdr->amax_w_bits;
+                a.row_map = crow + r0;
+                a.dyn_rows = nvc + c;
                 LCE_LAUNCH(PK_GRADX, launch_gemm(MODE_GRADX, mG_k, mW16_mn, a, grid_for(static_cast<int64_t>(a.m_tiles) * a.n_tiles), s));
             }
             {   // grad_W_acc (+)= s P^T X_c
@@ -379,6 +394,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.acc_first = first;
                 a.write_bf16 = last && o.grad_W != nullptr;
                 a.b_amax_bits = &hdr->amax_x_bits;
+                a.dyn_rows = nvc + c;
                 LCE_LAUNCH(PK_GRADW, launch_gemm(MODE_GRADW, mG_mn, mX16_mn, a, grid_for(static_cast<int64_t>(a.m_tiles) * a.n_tiles), s));
             }
             // grad_W_acc[y_i] -= s X[i] for the chunk's valid rows, exactly, in row order

@@ -101,15 +101,18 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 }
 
 // The fused path's softmax without recomputing the logits: the forward
-// stored E = fp16(2^(t - m) 2^15) per (row, 256-column vocab tile) with m the
-// tile's max; here, once lse is known, P = fp16(E 2^(m - lse log2 e)) in
-// place (= fp16(p 2^15)), 0 for ignored rows.  One block covers 32 rows of
-// one vocab tile: 32 threads x 8 columns, 8 rows at a time.  With gb_part,
-// it also writes the block's fp32 column sums of p (row order fixed).
+// stored E = fp16(2^(t - m) 2^15) per (valid row, 256-column vocab tile),
+// with m the tile's max, at the row's compacted position; here, once lse is
+// known, P = fp16(E 2^(m - lse log2 e)) in place (= fp16(p 2^15)).  Compact
+// rows from n_valid up to the next multiple of 64 are zeroed (the K tail of
+// the grad_W product).  One block covers 32 compact rows of one vocab tile:
+// 32 threads x 8 columns, 8 rows at a time.  With gb_part it also writes the
+// block's fp32 column sums of p (fixed row order).
 __global__ void __launch_bounds__(256) p_rescale_kernel(uint16_t* __restrict__ P, int64_t ldg, int64_t rows,
                                                         int64_t V, const float* __restrict__ pm, int64_t ldp,
                                                         const float* __restrict__ lse,
-                                                        const int64_t* __restrict__ y, int64_t ignore_index,
+                                                        const int* __restrict__ crow,
+                                                        const int* __restrict__ n_valid,
                                                         float* __restrict__ gb_part) {
     __shared__ float colsum[8][256 + 4];
     constexpr float LOG2E = 1.4426950408889634f;
@@ -119,17 +122,22 @@ __global__ void __launch_bounds__(256) p_rescale_kernel(uint16_t* __restrict__ P
     const int64_t c = tile * 256 + cg * 8;
     const int64_t cend = (tile * 256 + 256 < ldg) ? tile * 256 + 256 : ldg;
     const bool col_ok = c < cend;
+    const int64_t nv = *n_valid;
+    const int64_t zero_end = (nv + 63) / 64 * 64;
     float sum[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) sum[k] = 0.f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const int64_t r = row0 + rr + 8 * q;
-        if (r >= rows || !col_ok) continue;
-        const int64_t yr = y[r];
-        const bool valid = yr != ignore_index && yr >= 0 && yr < V;
-        const float f = valid ? exp2f(pm[tile * ldp + r] - lse[r] * LOG2E) : 0.f;
-        uint4* ptr = reinterpret_cast<uint4*>(P + r * ldg + c);
+        const int64_t j = row0 + rr + 8 * q;  // compact row
+        if (j >= rows || !col_ok) continue;
+        uint4* ptr = reinterpret_cast<uint4*>(P + j * ldg + c);
+        if (j >= nv) {
+            if (j < zero_end) *ptr = make_uint4(0u, 0u, 0u, 0u);
+            continue;
+        }
+        const int64_t r = crow[j];  // chunk row
+        const float f = exp2f(pm[tile * ldp + r] - lse[r] * LOG2E);
         const uint4 w = *ptr;
         const uint32_t u[4] = {w.x, w.y, w.z, w.w};
         uint32_t o[4];
@@ -155,6 +163,98 @@ __global__ void __launch_bounds__(256) p_rescale_kernel(uint16_t* __restrict__ P
 #pragma unroll
         for (int k = 0; k < 8; ++k) t += colsum[k][threadIdx.x];
         gb_part[blockIdx.x * V + v] = t * (1.f / static_cast<float>(1 << P_SCALE_EXP));
+    }
+}
+
+// Valid-row compaction of every chunk: dmap[row] = the row's position among
+// its chunk's valid rows (-1 for an ignored or out-of-range label), crow[chunk
+// start + position] = the row (relative to the chunk), n_valid[chunk] = count.
+// One block per chunk scans its rows in order, 1024 at a time.
+__global__ void __launch_bounds__(1024) compact_rows_kernel(const int64_t* __restrict__ y, int64_t N, int64_t C,
+                                                            int64_t V, int64_t ignore_index, int* __restrict__ dmap,
+                                                            int* __restrict__ crow, int* __restrict__ n_valid) {
+    __shared__ int warp_total[32];
+    __shared__ int running;
+    const int64_t c = blockIdx.x;
+    const int64_t r0 = c * C;
+    const int64_t rows = (N - r0) < C ? (N - r0) : C;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (threadIdx.x == 0) running = 0;
+    __syncthreads();
+    for (int64_t base = 0; base < rows; base += blockDim.x) {
+        const int64_t i = base + threadIdx.x;
+        bool valid = false;
+        if (i < rows) {
+            const int64_t v = y[r0 + i];
+            valid = v != ignore_index && v >= 0 && v < V;
+        }
+        const unsigned ballot = __ballot_sync(0xFFFFFFFFu, valid);
+        const int before_in_warp = __popc(ballot & ((1u << lane) - 1u));
+        if (lane == 0) warp_total[w] = __popc(ballot);
+        __syncthreads();
+        int before_warp = 0;
+        for (int k = 0; k < w; ++k) before_warp += warp_total[k];
+        const int d = running + before_warp + before_in_warp;
+        if (i < rows) {
+            dmap[r0 + i] = valid ? d : -1;
+            if (valid) crow[r0 + d] = static_cast<int>(i);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int t = 0;
+            for (int k = 0; k < static_cast<int>(blockDim.x >> 5); ++k) t += warp_total[k];
+            running += t;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) n_valid[c] = running;
+}
+
+// grad_X rows of ignored rows are zero (the compacted products never write them).
+__global__ void zero_ignored_rows_kernel(const int* __restrict__ dmap, int64_t N, int64_t H,
+                                         uint16_t* __restrict__ grad_X) {
+    for (int64_t r = blockIdx.x; r < N; r += gridDim.x) {
+        if (dmap[r] >= 0) continue;
+        uint4* row = reinterpret_cast<uint4*>(grad_X + r * H);
+        for (int64_t k = threadIdx.x; k < H / 8; k += blockDim.x) row[k] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// X16[j] = fp16(X[crow[j]] 2^k) for the chunk's valid rows in compacted order
+// (k from max |X|), zero rows from n_valid to the next multiple of 64; with
+// P_tail, the same tail rows of P are zeroed too.
+__global__ void gather_f16_kernel(const uint16_t* __restrict__ X_chunk, int64_t H, const int* __restrict__ crow,
+                                  const int* __restrict__ n_valid, int64_t max_rows, const unsigned* amax_bits,
+                                  uint16_t* __restrict__ X16, uint16_t* __restrict__ P_tail, int64_t ldg) {
+    const float f = ldexpf(1.f, operand_scale_exp(*amax_bits));
+    const int64_t nv = *n_valid;
+    int64_t end = (nv + 63) / 64 * 64;
+    if (end > max_rows) end = max_rows;
+    const int64_t h8 = H / 8;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < end * h8; e += stride) {
+        const int64_t j = e / h8, k = e - j * h8;
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (j < nv) {
+            const uint4 w = reinterpret_cast<const uint4*>(X_chunk + static_cast<int64_t>(crow[j]) * H)[k];
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+            uint32_t r[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                __half2 hh = __floats2half2_rn(__uint_as_float(u[q] << 16) * f, __uint_as_float(u[q] & 0xFFFF0000u) * f);
+                r[q] = *reinterpret_cast<uint32_t*>(&hh);
+            }
+            o = make_uint4(r[0], r[1], r[2], r[3]);
+        }
+        reinterpret_cast<uint4*>(X16 + j * H)[k] = o;
+    }
+    if (P_tail) {
+        const int64_t g8 = ldg / 8;
+        for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < (end - nv) * g8;
+             e += stride) {
+            const int64_t j = nv + e / g8, k = e % g8;
+            reinterpret_cast<uint4*>(P_tail + j * ldg)[k] = make_uint4(0u, 0u, 0u, 0u);
+        }
     }
 }
 
@@ -555,12 +655,34 @@ cudaError_t launch_to_f16_scaled(const uint16_t* x, int64_t n, const unsigned* a
 }
 
 cudaError_t launch_p_rescale(uint16_t* P, int64_t ldg, int64_t rows, int64_t V, const float* pm, int64_t ldp,
-                             const float* lse, const int64_t* y, int64_t ignore_index, float* gb_part,
+                             const float* lse, const int* crow, const int* n_valid, float* gb_part,
                              cudaStream_t s) {
     // every 32-row block of every 128-row tile writes its column sums (zeros
     // past the last row), the layout the grad_b accumulation reads
     const dim3 grid(static_cast<unsigned>((rows + 127) / 128 * 4), static_cast<unsigned>((V + 255) / 256));
-    p_rescale_kernel<<<grid, 256, 0, s>>>(P, ldg, rows, V, pm, ldp, lse, y, ignore_index, gb_part);
+    p_rescale_kernel<<<grid, 256, 0, s>>>(P, ldg, rows, V, pm, ldp, lse, crow, n_valid, gb_part);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_compact_rows(const int64_t* y, int64_t N, int64_t C, int64_t n_chunks, int64_t V,
+                                int64_t ignore_index, int* dmap, int* crow, int* n_valid_chunk, cudaStream_t s) {
+    compact_rows_kernel<<<static_cast<unsigned>(n_chunks), 1024, 0, s>>>(y, N, C, V, ignore_index, dmap, crow,
+                                                                         n_valid_chunk);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_zero_ignored_rows(const int* dmap, int64_t N, int64_t H, uint16_t* grad_X, cudaStream_t s) {
+    const int64_t want = N < 8192 ? N : 8192;
+    zero_ignored_rows_kernel<<<static_cast<unsigned>(want), 128, 0, s>>>(dmap, N, H, grad_X);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_f16(const uint16_t* X_chunk, int64_t H, const int* crow, const int* n_valid,
+                              int64_t max_rows, const unsigned* amax_bits, uint16_t* X16, uint16_t* P_tail,
+                              int64_t ldg, cudaStream_t s) {
+    const int64_t want = (max_rows * (H / 8) + 255) / 256;
+    const int blocks = static_cast<int>(want < 1 ? 1 : (want < 4096 ? want : 4096));
+    gather_f16_kernel<<<blocks, 256, 0, s>>>(X_chunk, H, crow, n_valid, max_rows, amax_bits, X16, P_tail, ldg);
     return cudaGetLastError();
 }
 

@@ -179,12 +179,18 @@ __device__ __forceinline__ float warp_column_sums(float (&g)[32], int lane) {
     return g[0];
 }
 
+// m_rows: rows of the output that exist (a.M, or the compacted row count);
+// zero_acc: the tile had no K work (an empty compacted chunk), so its
+// accumulator reads as zero.
 template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, int q, int lane,
-                                              uint32_t taddr, uint32_t empty_bar) {
+                                              uint32_t taddr, uint32_t empty_bar, int64_t m_rows,
+                                              bool zero_acc) {
     const int64_t row = static_cast<int64_t>(m) * BM + q * 32 + lane;
     const int64_t col0 = static_cast<int64_t>(n) * BN;
-    const bool row_ok = row < a.M;
+    const bool row_ok = row < m_rows;
+    // MODE_LSE / MODE_G: where this row's E or P row goes (-1: not stored)
+    const int64_t prow = (a.row_map && row_ok) ? static_cast<int64_t>(a.row_map[row]) : (row_ok ? row : -1);
 
     if constexpr (MODE == MODE_LSE) {
         // Two passes over the tile's TMEM row.  Pass 1: the tile max of
@@ -226,7 +232,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
                 sm += e;
                 v[i] = e * P_SCALE;
             }
-            if (a.g && row_ok) store_f16_32(a.g + row * a.ldg + c0, v, static_cast<int>(min64(32, a.ldg - c0)));
+            if (a.g && prow >= 0) store_f16_32(a.g + prow * a.ldg + c0, v, static_cast<int>(min64(32, a.ldg - c0)));
         }
         tc_fence_before_sync();
         __syncwarp();
@@ -253,11 +259,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
                 const float p = fast_exp2(fmaf(v[i], LOG2E_F, -lse2));
                 v[i] = (valid && i < nv) ? p : 0.f;
             }
-            if (row_ok) {
+            if (prow >= 0) {
                 float ps[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) ps[i] = v[i] * P_SCALE;
-                store_f16_32(a.g + row * a.ldg + c0, ps, static_cast<int>(min64(32, a.ldg - c0)));
+                store_f16_32(a.g + prow * a.ldg + c0, ps, static_cast<int>(min64(32, a.ldg - c0)));
             }
             if (a.gb_part) {
                 const float cs = warp_column_sums(v, lane);
@@ -271,7 +277,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         // grad_X[i] = s (sum_v P[i,v] W[v] - W[y_i]); P rows of ignored rows are 0
         const float s = *a.scale;
         const float f = ldexpf(s, -(P_SCALE_EXP + operand_scale_exp(*a.b_amax_bits)));
-        const int64_t yr = row_ok ? a.y[row] : a.ignore_index;
+        const int64_t orow = (a.row_map && row_ok) ? static_cast<int64_t>(a.row_map[row]) : row;  // chunk row
+        const int64_t yr = row_ok ? a.y[orow] : a.ignore_index;
         const bool valid = row_ok && yr != a.ignore_index && yr >= 0 && yr < a.V;
         const uint16_t* wy = a.w_rows + (valid ? yr : 0) * a.ldw;
 #pragma unroll 1
@@ -292,7 +299,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= f;
                 }
-                store_bf16_32(a.out_bf16 + row * a.ld_out + c0, v, static_cast<int>(min64(32, a.N - c0)));
+                store_bf16_32(a.out_bf16 + orow * a.ld_out + c0, v, static_cast<int>(min64(32, a.N - c0)));
             }
         }
         tc_fence_before_sync();
@@ -306,6 +313,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
             if (c0 >= a.N) break;
             float v[32];
             tmem_load_32cols(taddr + 32 * j, v);
+            if (zero_acc) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            }
             if (row_ok) {
                 float* p = a.out_f32 + row * a.ld_f32 + c0;
                 if (a.acc_first) {
@@ -385,6 +396,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = ctl->tmem_base;
     const int num_tiles = args.m_tiles * args.n_tiles;
+    // Compacted row count (written by an earlier kernel): limits the row tiles
+    // of MODE_GRADX and the K loop of MODE_GRADW.  Every role reads the same
+    // value, so all three skip the same tiles and run the same K loops.
+    const int dyn = args.dyn_rows ? *args.dyn_rows : -1;
+    const int64_t m_rows = (MODE == MODE_GRADX && dyn >= 0) ? static_cast<int64_t>(dyn) : args.M;
+    const int k_blocks = (MODE == MODE_GRADW && dyn >= 0) ? (dyn + BK - 1) / BK : args.k_blocks;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -395,7 +412,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 int m, n;
                 tile_coords(t, args, m, n);
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                if (static_cast<int64_t>(m) * BM >= m_rows) continue;
+                for (int kb = 0; kb < k_blocks; ++kb) {
                     if (!wait_phase(smem_u32(&ctl->empty[stage]), phase ^ 1u, ctl, args.status, limit)) {
                         ok = false;
                         break;
@@ -447,13 +465,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                int m, n;
+                tile_coords(t, args, m, n);
+                if (static_cast<int64_t>(m) * BM >= m_rows) continue;
                 if (!wait_phase(smem_u32(&ctl->tmem_empty[acc]), acc_phase ^ 1u, ctl, args.status, limit)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                for (int kb = 0; kb < k_blocks; ++kb) {
                     if (!wait_phase(smem_u32(&ctl->full[stage]), phase, ctl, args.status, limit)) {
                         ok = false;
                         break;
@@ -491,10 +512,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             int m, n;
             tile_coords(t, args, m, n);
+            if (static_cast<int64_t>(m) * BM >= m_rows) continue;
             if (!wait_phase(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, args.status, limit)) break;
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            epilogue_tile<MODE>(args, m, n, q, lane, taddr, smem_u32(&ctl->tmem_empty[acc]));
+            epilogue_tile<MODE>(args, m, n, q, lane, taddr, smem_u32(&ctl->tmem_empty[acc]), m_rows, k_blocks == 0);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }

@@ -113,6 +113,15 @@ struct GemmArgs {
     int64_t ld_f32;
     int32_t acc_first;   // MODE_GRADW: overwrite instead of accumulate
     int32_t write_bf16;  // MODE_GRADW: also write the bf16 cast
+    // Valid-row compaction: the backward products skip ignored rows.
+    //   MODE_LSE / MODE_G: row_map[chunk row] = row of the compacted P it is
+    //     stored at (-1: ignored, not stored).
+    //   MODE_GRADX: row_map[compact row] = chunk row; dyn_rows = number of
+    //     compact rows (the M extent; row tiles past it are skipped).
+    //   MODE_GRADW: dyn_rows = number of compact rows (the K extent).
+    // Both nullable (no compaction).
+    const int* row_map;
+    const int* dyn_rows;
     unsigned* status;
     uint64_t timeout_ns;
 };
@@ -151,11 +160,17 @@ cudaError_t launch_grad_b(const float* gb_part, int64_t parts, int64_t V, const 
                           int last, cudaStream_t s);
 cudaError_t launch_wait_probe(unsigned* status, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_p_rescale(uint16_t* P, int64_t ldg, int64_t rows, int64_t V, const float* pm, int64_t ldp,
-                             const float* lse, const int64_t* y, int64_t ignore_index, float* gb_part,
+                             const float* lse, const int* crow, const int* n_valid, float* gb_part,
                              cudaStream_t s);
 cudaError_t launch_scale_grads(int64_t N, int64_t H, int64_t V, const float* d_grad_output, uint16_t* grad_X,
                                const float* grad_W_acc, uint16_t* grad_W, const float* grad_b_acc,
                                uint16_t* grad_b, cudaStream_t s);
+cudaError_t launch_compact_rows(const int64_t* y, int64_t N, int64_t C, int64_t n_chunks, int64_t V,
+                                int64_t ignore_index, int* dmap, int* crow, int* n_valid_chunk, cudaStream_t s);
+cudaError_t launch_zero_ignored_rows(const int* dmap, int64_t N, int64_t H, uint16_t* grad_X, cudaStream_t s);
+cudaError_t launch_gather_f16(const uint16_t* X_chunk, int64_t H, const int* crow, const int* n_valid,
+                              int64_t max_rows, const unsigned* amax_bits, uint16_t* X16, uint16_t* P_tail,
+                              int64_t ldg, cudaStream_t s);
 cudaError_t launch_amax(const uint16_t* x, int64_t n, unsigned* amax_bits, cudaStream_t s);
 cudaError_t launch_to_f16_scaled(const uint16_t* x, int64_t n, const unsigned* amax_bits, uint16_t* out,
                                  cudaStream_t s);
