@@ -298,6 +298,38 @@ def run_ours(args, w):
         raise RuntimeError(f"device status after timed steps: {lce.STATUS[st]}")
     t_step = max_over_ranks(t_step)
 
+    # ---- the forward and the backward entry points on their own (2NHV and 6NHV)
+    split = None
+    if not args.no_split:
+        nws_f = lce.lce_workspace_size(N, H, V, chunk, False, lce.WS_FORWARD)
+        nws_b = lce.lce_workspace_size(N, H, V, chunk, False, lce.WS_BACKWARD)
+        ws_f = torch.empty(nws_f, dtype=torch.uint8, device=dev)
+        ws_b = torch.empty(nws_b, dtype=torch.uint8, device=dev)
+
+        def fwd():
+            lce.lce_forward(N, H, V, X, W, None, y, -100, chunk, loss, lse, n_valid, ws_f, nws_f, s)
+
+        def bwd():
+            lce.lce_backward(N, H, V, X, W, None, y, -100, chunk, lse, 1.0, None, gX, gW, None, gW_acc, None,
+                             ws_b, nws_b, s)
+
+        split = {}
+        for name, fn, fl in (("forward", fwd, 2.0 * N * H * V), ("backward", bwd, 6.0 * N * H * V)):
+            for _ in range(2):
+                fn()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(s)
+            for _ in range(args.steps):
+                fn()
+            a1.record(s)
+            torch.cuda.synchronize(dev)
+            t = a0.elapsed_time(a1) / 1e3 / args.steps
+            split[name] = {"ms": 1e3 * t, "tokens_per_s": N / t, "tflops": fl / t / 1e12}
+        st = lce.lce_check_status(ws_b, s)
+        if st != 0:
+            raise RuntimeError(f"device status after lce_backward: {lce.STATUS[st]}")
+        del ws_f, ws_b
+
     # ---- end to end: host buffers, copies inside the timed region.  Two sets
     # of device buffers: step k+1's inputs are copied in while step k
     # computes, and step k's results are copied out while step k+1 computes.
@@ -431,6 +463,7 @@ def run_ours(args, w):
         "logits_bytes_avoided": N * V * 2,
         "clocks": clocks,
         "e2e": e2e,
+        "separate_entry_points": split,
     }
     if not args.no_cpu_baseline and ws_n == 1:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_rows)
@@ -483,6 +516,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=32, help="rows per step of --impl reference")
     ap.add_argument("--gemm", default=None, help="M,N,K,layout: time the bare GEMM core instead")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-split", action="store_true", help="skip timing lce_forward and lce_backward alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -12,6 +12,9 @@
 namespace lce {
 namespace {
 
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
 constexpr int64_t AUTO_CHUNK_ROWS = 16384;
 // Tile-order groups: 32 row tiles of X (4096 rows, 32 MB at H = 4096) for
 // the logits passes; for the grad_W pass, as many 256-column tiles of the
@@ -19,20 +22,34 @@ constexpr int64_t AUTO_CHUNK_ROWS = 16384;
 constexpr int32_t LOGITS_GROUP_M = 32;
 constexpr int64_t GROUP_BYTES = 32ll << 20;
 
+// grad_X of a chunk with few output tiles (e.g. 256-row chunks) is split
+// over K (the vocabulary) so that about two waves of tiles fill the GPU;
+// the target does not depend on the device, so neither does the workspace.
+constexpr int64_t GRADX_TARGET_TILES = 304;
+
+int64_t gradx_splits(int64_t C, int64_t H, int64_t V) {
+    const int64_t tiles = cdiv(C, BM) * cdiv(H, BN);
+    if (tiles >= GRADX_TARGET_TILES / 2) return 1;
+    int64_t s = cdiv(GRADX_TARGET_TILES, tiles);
+    const int64_t kb = cdiv(V, BK);
+    if (s > kb / 4) s = kb / 4;
+    if (s > 64) s = 64;
+    if (s <= 1) return 1;
+    return cdiv(kb, cdiv(kb, s));  // every slice gets at least one k-block
+}
+
 int32_t gradw_group_n(int64_t rows) {
     const int64_t g = GROUP_BYTES / (rows * BN * 2);
     return static_cast<int32_t>(g < 1 ? 1 : (g > 64 ? 64 : g));
 }
 constexpr size_t HEADER_BYTES = 1024;
 
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct Plan {
-    int64_t N, H, V, C, n_chunks, n_vt, ldg, mt_chunk, label_blocks_per_chunk;
+    int64_t N, H, V, C, n_chunks, n_vt, ldg, mt_chunk, label_blocks_per_chunk, gradx_splits;
     bool has_bias;
     size_t off_row_loss, off_zt, off_pm, off_ps, off_g, off_gb, off_keys, off_runs, off_nrun, off_counts, off_w16,
-        off_x16, off_dmap, off_crow, off_nvc, total;
+        off_x16, off_dmap, off_crow, off_nvc, off_split, total;
 };
 
 lce_status_t check_sizes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows) {
@@ -60,6 +77,7 @@ lce_status_t make_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, bool
     p->ldg = align_up(static_cast<size_t>(V), 8);
     p->mt_chunk = cdiv(p->C, BM);
     p->label_blocks_per_chunk = cdiv(p->C, LABEL_BLOCK);
+    p->gradx_splits = gradx_splits(p->C, H, V);
     p->has_bias = has_bias;
     const bool fwd = which != LCE_WS_BACKWARD, bwd = which != LCE_WS_FORWARD;
     size_t off = HEADER_BYTES;
@@ -84,6 +102,7 @@ lce_status_t make_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, bool
     p->off_dmap = take(bwd, static_cast<size_t>(N) * 4);
     p->off_crow = take(bwd, static_cast<size_t>(N) * 4);
     p->off_nvc = take(bwd, static_cast<size_t>(p->n_chunks) * 4);
+    p->off_split = take(bwd && p->gradx_splits > 1, static_cast<size_t>(p->gradx_splits) * p->C * H * 4);
     p->total = off;
     return LCE_OK;
 }
@@ -148,6 +167,7 @@ GemmArgs base_args(WsHeader* hdr) {
     memset(&a, 0, sizeof(a));
     a.group_m = 1;
     a.group_n = 1;
+    a.k_splits = 1;
     a.status = &hdr->status;
     a.timeout_ns = WAIT_LIMIT_NS;
     return a;
@@ -264,6 +284,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     int* dmap = do_bwd ? reinterpret_cast<int*>(wsb + p.off_dmap) : nullptr;  // row -> compacted row or -1
     int* crow = do_bwd ? reinterpret_cast<int*>(wsb + p.off_crow) : nullptr;  // compacted row -> chunk row
     int* nvc = do_bwd ? reinterpret_cast<int*>(wsb + p.off_nvc) : nullptr;    // valid rows per chunk
+    float* split_out = (do_bwd && p.gradx_splits > 1) ? reinterpret_cast<float*>(wsb + p.off_split) : nullptr;
     int* counts = (do_bwd && pb.b) ? reinterpret_cast<int*>(wsb + p.off_counts) : nullptr;
 
     // operand maps of the whole X and W
@@ -375,7 +396,17 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.b_amax_bits = &hdr->amax_w_bits;
                 a.row_map = crow + r0;
                 a.dyn_rows = nvc + c;
-                LCE_LAUNCH(PK_GRADX, launch_gemm(MODE_GRADX, mG_k, mW16_mn, a, grid_for(static_cast<int64_t>(a.m_tiles) * a.n_tiles), s));
+                a.k_splits = static_cast<int32_t>(p.gradx_splits);
+                a.k_per_split = static_cast<int32_t>(cdiv(a.k_blocks, p.gradx_splits));
+                a.split_out = split_out;
+                a.split_stride = p.C * pb.H;
+                LCE_LAUNCH(PK_GRADX, launch_gemm(MODE_GRADX, mG_k, mW16_mn, a,
+                                                 grid_for(static_cast<int64_t>(a.m_tiles) * a.n_tiles * p.gradx_splits),
+                                                 s));
+                if (split_out)
+                    LCE_LAUNCH(PK_GRADX, launch_gradx_split_reduce(split_out, p.gradx_splits, p.C * pb.H, pb.H, crow + r0,
+                                                                   nvc + c, rows, pb.y + r0, pb.ignore_index, pb.V,
+                                                                   pb.W, hdr, o.grad_X + r0 * pb.H, s));
             }
             {   // grad_W_acc (+)= s P^T X_c
                 GemmArgs a = base_args(hdr);

@@ -496,6 +496,57 @@ __global__ void scale_grads_kernel(int64_t nx8, int64_t nw8, int64_t V, const fl
         }
 }
 
+// Finishes a split grad_X product: for each compacted row j < n_valid and
+// column h, sum the K slices' partial sums in slice order, then
+// grad_X[crow[j], h] = s (2^-(15+k_W) sum - W[y, h]) as bf16 (the same
+// arithmetic as the unsplit epilogue).
+__global__ void gradx_split_reduce_kernel(const float* __restrict__ split_out, int64_t splits, int64_t split_stride,
+                                          int64_t H, const int* __restrict__ crow, const int* __restrict__ n_valid,
+                                          const int64_t* __restrict__ y, int64_t ignore_index, int64_t V,
+                                          const uint16_t* __restrict__ W, const WsHeader* hdr,
+                                          uint16_t* __restrict__ grad_X_chunk) {
+    const float s = hdr->scale;
+    const float f = ldexpf(s, -(P_SCALE_EXP + operand_scale_exp(hdr->amax_w_bits)));
+    const int64_t nv = *n_valid, h8 = H / 8;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < nv * h8; e += stride) {
+        const int64_t j = e / h8, h = (e - j * h8) * 8;
+        float sum[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sum[k] = 0.f;
+        for (int64_t ks = 0; ks < splits; ++ks) {
+            const float* src = split_out + ks * split_stride + j * H + h;
+            const float4 a = *reinterpret_cast<const float4*>(src);
+            const float4 b = *reinterpret_cast<const float4*>(src + 4);
+            sum[0] += a.x; sum[1] += a.y; sum[2] += a.z; sum[3] += a.w;
+            sum[4] += b.x; sum[5] += b.y; sum[6] += b.z; sum[7] += b.w;
+        }
+        const int64_t r = crow[j];
+        const int64_t yr = y[r];
+        float w[8];
+        if (yr != ignore_index && yr >= 0 && yr < V) {
+            const uint4 q = *reinterpret_cast<const uint4*>(W + yr * H + h);
+            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                w[2 * k] = __uint_as_float(u[k] << 16);
+                w[2 * k + 1] = __uint_as_float(u[k] & 0xFFFF0000u);
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = 0.f;
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(fmaf(f, sum[2 * k], -s * w[2 * k]),
+                                                      fmaf(f, sum[2 * k + 1], -s * w[2 * k + 1]));
+            o[k] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+        *reinterpret_cast<uint4*>(grad_X_chunk + r * H + h) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 // max |x| over bf16 values, as float bits (non-negative floats order like
 // their bit patterns, so an integer max is exact and order-independent).
 __global__ void amax_kernel(const uint16_t* __restrict__ x, int64_t n, unsigned* amax_bits) {
@@ -697,6 +748,17 @@ cudaError_t launch_scale_grads(int64_t N, int64_t H, int64_t V, const float* d_g
                                               reinterpret_cast<uint4*>(grad_X),
                                               reinterpret_cast<const float4*>(grad_W_acc),
                                               reinterpret_cast<uint4*>(grad_W), grad_b_acc, grad_b);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gradx_split_reduce(const float* split_out, int64_t splits, int64_t split_stride, int64_t H,
+                                      const int* crow, const int* n_valid, int64_t max_rows, const int64_t* y,
+                                      int64_t ignore_index, int64_t V, const uint16_t* W, const WsHeader* hdr,
+                                      uint16_t* grad_X_chunk, cudaStream_t s) {
+    const int64_t want = (max_rows * (H / 8) + 255) / 256;
+    const int blocks = static_cast<int>(want < 1 ? 1 : (want < 4096 ? want : 4096));
+    gradx_split_reduce_kernel<<<blocks, 256, 0, s>>>(split_out, splits, split_stride, H, crow, n_valid, y,
+                                                     ignore_index, V, W, hdr, grad_X_chunk);
     return cudaGetLastError();
 }
 

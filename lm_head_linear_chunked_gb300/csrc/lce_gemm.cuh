@@ -93,6 +93,13 @@ __device__ __forceinline__ void tile_coords(int t, const GemmArgs& a, int& m, in
     }
 }
 
+// Tile t of a launch: output tile (m, n) and K slice ks (0 without a split).
+__device__ __forceinline__ void tile_and_slice(int t, const GemmArgs& a, int& m, int& n, int& ks) {
+    const int per = a.m_tiles * a.n_tiles;
+    ks = t / per;
+    tile_coords(t - ks * per, a, m, n);
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -185,7 +192,7 @@ __device__ __forceinline__ float warp_column_sums(float (&g)[32], int lane) {
 template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, int q, int lane,
                                               uint32_t taddr, uint32_t empty_bar, int64_t m_rows,
-                                              bool zero_acc) {
+                                              bool zero_acc, int ks) {
     const int64_t row = static_cast<int64_t>(m) * BM + q * 32 + lane;
     const int64_t col0 = static_cast<int64_t>(n) * BN;
     const bool row_ok = row < m_rows;
@@ -274,6 +281,26 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar);
     } else if constexpr (MODE == MODE_GRADX) {
+      if (a.k_splits > 1) {
+        // one K slice of a split product: the raw fp32 partial sums, finished
+        // by the reduction kernel (fixed slice order)
+        float* dst = a.split_out + static_cast<int64_t>(ks) * a.split_stride;
+#pragma unroll 1
+        for (int j = 0; j < BN / 32; ++j) {
+            const int64_t c0 = col0 + 32 * j;
+            if (c0 >= a.N) break;
+            float v[32];
+            tmem_load_32cols(taddr + 32 * j, v);
+            if (zero_acc) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            }
+            if (row_ok) store_f32_32(dst + row * a.N + c0, v, static_cast<int>(min64(32, a.N - c0)));
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar);
+      } else {
         // grad_X[i] = s (sum_v P[i,v] W[v] - W[y_i]); P rows of ignored rows are 0
         const float s = *a.scale;
         const float f = ldexpf(s, -(P_SCALE_EXP + operand_scale_exp(*a.b_amax_bits)));
@@ -305,6 +332,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar);
+      }
     } else if constexpr (MODE == MODE_GRADW) {
         const float s = ldexpf(*a.scale, -(P_SCALE_EXP + operand_scale_exp(*a.b_amax_bits)));
 #pragma unroll 1
@@ -395,7 +423,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = ctl->tmem_base;
-    const int num_tiles = args.m_tiles * args.n_tiles;
+    const int num_tiles = args.m_tiles * args.n_tiles * (args.k_splits > 1 ? args.k_splits : 1);
     // Compacted row count (written by an earlier kernel): limits the row tiles
     // of MODE_GRADX and the K loop of MODE_GRADW.  Every role reads the same
     // value, so all three skip the same tiles and run the same K loops.
@@ -410,10 +438,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             uint64_t issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                int m, n;
-                tile_coords(t, args, m, n);
+                int m, n, ks;
+                tile_and_slice(t, args, m, n, ks);
                 if (static_cast<int64_t>(m) * BM >= m_rows) continue;
-                for (int kb = 0; kb < k_blocks; ++kb) {
+                const int kb0 = args.k_splits > 1 ? ks * args.k_per_split : 0;
+                const int kb1 = args.k_splits > 1 ? min(k_blocks, kb0 + args.k_per_split) : k_blocks;
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase(smem_u32(&ctl->empty[stage]), phase ^ 1u, ctl, args.status, limit)) {
                         ok = false;
                         break;
@@ -465,16 +495,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                int m, n;
-                tile_coords(t, args, m, n);
+                int m, n, ks;
+                tile_and_slice(t, args, m, n, ks);
                 if (static_cast<int64_t>(m) * BM >= m_rows) continue;
+                const int kb0 = args.k_splits > 1 ? ks * args.k_per_split : 0;
+                const int kb1 = args.k_splits > 1 ? min(k_blocks, kb0 + args.k_per_split) : k_blocks;
                 if (!wait_phase(smem_u32(&ctl->tmem_empty[acc]), acc_phase ^ 1u, ctl, args.status, limit)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < k_blocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase(smem_u32(&ctl->full[stage]), phase, ctl, args.status, limit)) {
                         ok = false;
                         break;
@@ -487,7 +519,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
                         mma_f16kind(d_tmem, adesc + A_STEP * k, bdesc + B_STEP * k, IDESC,
-                                     (kb | k) != 0 ? 1u : 0u);
+                                     (kb != kb0 || k != 0) ? 1u : 0u);
                     mma_commit(smem_u32(&ctl->empty[stage]));
                     if (++stage == STAGES) {
                         stage = 0;
@@ -510,13 +542,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int q = warp & 3;
         uint32_t acc = 0, acc_phase = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-            int m, n;
-            tile_coords(t, args, m, n);
+            int m, n, ks;
+            tile_and_slice(t, args, m, n, ks);
             if (static_cast<int64_t>(m) * BM >= m_rows) continue;
+            const int kb0 = args.k_splits > 1 ? ks * args.k_per_split : 0;
+            const int kb1 = args.k_splits > 1 ? min(k_blocks, kb0 + args.k_per_split) : k_blocks;
             if (!wait_phase(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, args.status, limit)) break;
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            epilogue_tile<MODE>(args, m, n, q, lane, taddr, smem_u32(&ctl->tmem_empty[acc]), m_rows, k_blocks == 0);
+            epilogue_tile<MODE>(args, m, n, q, lane, taddr, smem_u32(&ctl->tmem_empty[acc]), m_rows, kb1 <= kb0,
+                                ks);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }

@@ -122,6 +122,15 @@ struct GemmArgs {
     // Both nullable (no compaction).
     const int* row_map;
     const int* dyn_rows;
+    // MODE_GRADX split over K (for chunks with few output tiles): tile index
+    // t -> (m, n) = the raster of t % (m_tiles n_tiles), K slice
+    // t / (m_tiles n_tiles) of k_per_split k-blocks; the raw fp32 accumulator
+    // goes to split_out[slice][row][col] (row stride N, slice stride
+    // split_stride) and a reduction kernel finishes grad_X.  1 = no split.
+    int32_t k_splits;
+    int32_t k_per_split;
+    float* split_out;
+    int64_t split_stride;
     unsigned* status;
     uint64_t timeout_ns;
 };
@@ -171,6 +180,10 @@ cudaError_t launch_zero_ignored_rows(const int* dmap, int64_t N, int64_t H, uint
 cudaError_t launch_gather_f16(const uint16_t* X_chunk, int64_t H, const int* crow, const int* n_valid,
                               int64_t max_rows, const unsigned* amax_bits, uint16_t* X16, uint16_t* P_tail,
                               int64_t ldg, cudaStream_t s);
+cudaError_t launch_gradx_split_reduce(const float* split_out, int64_t splits, int64_t split_stride, int64_t H,
+                                      const int* crow, const int* n_valid, int64_t max_rows, const int64_t* y,
+                                      int64_t ignore_index, int64_t V, const uint16_t* W, const WsHeader* hdr,
+                                      uint16_t* grad_X_chunk, cudaStream_t s);
 cudaError_t launch_amax(const uint16_t* x, int64_t n, unsigned* amax_bits, cudaStream_t s);
 cudaError_t launch_to_f16_scaled(const uint16_t* x, int64_t n, const unsigned* amax_bits, uint16_t* out,
                                  cudaStream_t s);
