@@ -48,8 +48,9 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # workload, from the ncu capture summarised in
 # profiles/gemm_dram_full_qwen3-8b-head.md.  None once a kernel has changed
 # since its counters were taken.
-DRAM_BYTES_PER_LAUNCH = {"grad_w": 7.75e9 + 2.47e9, "grad_x": 11.70e9 + 0.06e9,
-                         "logits_lse": None, "recomputed_logits_softmax": None}
+DRAM_BYTES_PER_LAUNCH = {"grad_w": 23.07e9 + 2.47e9, "grad_x": 23.25e9 + 0.13e9,
+                         "logits_lse": 5.17e9 + 4.78e9, "recomputed_logits_softmax": None}
+DRAM_BYTES_CHUNK_ROWS = 16384  # the chunk size those launches ran with
 
 
 def load_peaks():
@@ -451,7 +452,7 @@ def run_ours(args, w):
         "roofline": {"bound": "tensor", "achieved": dom_tflops, "peak": sustained, "unit": "TFLOP/s",
                      "frac": dom_tflops / sustained,
                      "traffic": DRAM_BYTES_PER_LAUNCH.get(dom) if args.workload == WORKLOAD and not args.shape
-                     and C == 8192 else None,
+                     and C == DRAM_BYTES_CHUNK_ROWS else None,
                      "kernel": f"gemm_kernel ({dom})",
                      "flops_per_launch": dom_flops_per_launch, "launches": dom_n,
                      "mean_launch_ms": dom_ms / dom_n,
