@@ -11,6 +11,7 @@ at full size and in the launch configuration bench.py times:
   the sampled rows; for the Qwen3-0.6B-head workload the oracle also runs
   the whole forward and the loss is compared directly;
 * grad_W and grad_b: the 512 sampled rows are run as a problem of their own
+  (through lce_fused_fwd_bwd, and through lce_forward then lce_backward)
   and every output, including the full fp32 grad_W accumulator over all V
   rows, is compared with the oracle's;
 * the full-size accumulation over chunks: the rows split in two halves,
@@ -123,6 +124,14 @@ def test_sub_batch_all_outputs(problem):
     bb = problem.bits(problem.bh) if problem.bh is not None else None
     ref = oracle.fused(problem.bits(problem.Xh)[rows], Wb, bb, problem.y[rows], block_rows=512, threads=1)
     check_against_oracle(out, ref, has_bias=w.has_bias)
+    del out
+    # the same rows through lce_forward, then lce_backward (which recomputes the logits)
+    f = lce.forward(Xs, problem.W, problem.b, ys, chunk_rows=w.chunk_rows)
+    assert lce.lce_check_status(f["ws"], torch.cuda.current_stream()) == 0
+    check_against_oracle(f, ref, has_bias=w.has_bias, bwd=False)
+    g = lce.backward(Xs, problem.W, problem.b, ys, f["lse"], chunk_rows=w.chunk_rows)
+    assert lce.lce_check_status(g["ws"], torch.cuda.current_stream()) == 0
+    check_against_oracle(g, ref, has_bias=w.has_bias, fwd=False)
 
 
 def test_full_size_accumulation_is_additive(problem):
