@@ -6,6 +6,8 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "lce_internal.cuh"
 #include "lce_ptx.cuh"
 
@@ -628,15 +630,16 @@ cudaError_t launch_prepass(const int64_t* y, int64_t N, int64_t V, int64_t ignor
 cudaError_t launch_label_sort(const int64_t* y, int64_t N, int64_t C, int64_t blocks_per_chunk, int64_t n_blocks,
                               int64_t V, int64_t ignore_index, unsigned long long* keys, unsigned long long* runs,
                               int* run_count, cudaStream_t s) {
-    static int configured_device = -1;
+    static std::atomic<uint64_t> configured{0};  // bit d: shared-memory limit raised on device d
     constexpr int smem = LABEL_BLOCK * 8;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured_device != dev) {
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+    if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(label_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        configured_device = dev;
+        configured.fetch_or(bit, std::memory_order_release);
     }
     label_sort_kernel<<<static_cast<unsigned>(n_blocks), 1024, smem, s>>>(y, N, C, blocks_per_chunk, V,
                                                                           ignore_index, keys, runs, run_count);

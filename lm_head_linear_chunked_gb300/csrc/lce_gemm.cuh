@@ -19,6 +19,8 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "lce_internal.cuh"
 #include "lce_ptx.cuh"
 
@@ -567,15 +569,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 template <int MODE>
 cudaError_t launch_gemm_mode(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
                              int grid, cudaStream_t stream) {
-    static int configured_device = -1;
+    static std::atomic<uint64_t> configured{0};  // bit d: shared-memory limit raised on device d
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured_device != dev) {
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+    if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  GEMM_SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        configured_device = dev;
+        configured.fetch_or(bit, std::memory_order_release);
     }
     gemm_kernel<MODE><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(map_a, map_b, args);
     return cudaGetLastError();
