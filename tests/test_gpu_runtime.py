@@ -60,3 +60,33 @@ def test_side_stream_gives_the_same_bits():
     torch.cuda.synchronize()
     for k in ("loss", "lse", "gX", "gW", "acc"):
         assert bool((a[k].view(-1) == c[k].view(-1)).all().item()), k
+
+
+def test_cuda_graph_capture_and_replay():
+    """After one warm-up call (which loads the kernels and sets their
+    attributes), a fused call records into a CUDA graph; replays give the
+    eager call's bits."""
+    import torch
+    X, W, b, y = random_problem(43, 1536, 128, 4096, bias=False)
+    N, H, V = 1536, 128, 4096
+    Xd, Wd, yd = dev_bf16(X), dev_bf16(W), dev_i64(y)
+    eager, nws = _buffers(N, H, V, 512)
+    s = torch.cuda.current_stream()
+    _call(N, H, V, Xd, Wd, yd, 512, eager, nws, s)
+    assert lce.lce_check_status(eager["ws"], s) == 0
+    g_out, _ = _buffers(N, H, V, 512)
+    side = torch.cuda.Stream()
+    side.wait_stream(s)
+    with torch.cuda.stream(side):
+        _call(N, H, V, Xd, Wd, yd, 512, g_out, nws, side)   # warm-up on the capture stream
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        _call(N, H, V, Xd, Wd, yd, 512, g_out, nws, side)
+    for _ in range(2):
+        for k in ("loss", "lse", "gX", "gW", "acc"):
+            g_out[k].zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for k in ("loss", "lse", "gX", "gW", "acc"):
+            assert bool((eager[k].view(-1) == g_out[k].view(-1)).all().item()), k
