@@ -27,3 +27,16 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    path = os.environ.get("LCE_PARITY_REPORT")
+    if not path:
+        return
+    try:
+        from tests import gpu_util
+    except Exception:
+        return
+    import json
+    with open(path, "w") as f:
+        json.dump(gpu_util.RECORDS, f, indent=0)

@@ -4,6 +4,16 @@ from __future__ import annotations
 
 import numpy as np
 
+# (test, quantity, measured error, allowed error) of every check made in this
+# process; conftest writes them out when LCE_PARITY_REPORT names a file.
+RECORDS: list = []
+
+
+def _record(what, err, allowed):
+    import os
+    RECORDS.append({"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], "quantity": what,
+                    "error": float(err), "allowed": float(np.min(allowed)) if np.ndim(allowed) else float(allowed)})
+
 # Tolerances: loss relative 1e-4; lse absolute 1e-3; bf16 gradients max-abs
 # 1e-2 * max|ref|; fp32 accumulators max-abs 1e-4 * max|ref|.
 LOSS_RTOL = 1e-4
@@ -47,6 +57,7 @@ def assert_grad(got, ref, tol, what, elem_bound=None):
     if elem_bound is not None:
         allowed = np.maximum(allowed, elem_bound)
     bad = diff > allowed
+    _record(what, diff.max() if diff.size else 0.0, tol * max(scale, 1e-30))
     assert not bad.any() or (scale == 0 and diff.max() == 0), \
         f"{what}: max abs err {diff.max():.3e} > {tol:g} * max|ref| ({scale:.3e}) at {np.argwhere(bad)[0]}"
 
@@ -73,9 +84,11 @@ def check_against_oracle(out: dict, ref: dict, has_bias: bool, fwd=True, bwd=Tru
         loss = float(out["loss"].item())
         # relative 1e-4; the 1e-6 floor only matters for a loss near 0 (e.g.
         # V = 1), where fp32 rounding of lse = z leaves ~1e-10
+        _record("loss (relative)", abs(loss - ref["loss"]) / max(abs(ref["loss"]), 1e-30), LOSS_RTOL)
         assert abs(loss - ref["loss"]) <= LOSS_RTOL * abs(ref["loss"]) + 1e-6, f"loss {loss} vs oracle {ref['loss']}"
         lse = host_f64(out["lse"])
         err = np.abs(lse - ref["lse"]).max()
+        _record("lse (absolute)", err, LSE_ATOL)
         assert err <= LSE_ATOL, f"lse max abs err {err}"
         assert int(out["n_valid"].item()) == ref["n_valid"]
     if bwd:

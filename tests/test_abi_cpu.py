@@ -131,3 +131,23 @@ def test_debug_entry_points_host_errors():
         lce.lce_debug_wait_timeout(10, A, 8, None)
     assert e.value.status == 3
     assert lce.lce_check_status(None, None) == 1
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d_grad_output=None), 1), (dict(grad_W=None), 1), (dict(grad_b=A), 1), (dict(grad_X=A + 4), 1),
+    (dict(N=0), 1), (dict(H=12), 2),
+])
+def test_scale_grads_host_errors(kw, code):
+    args = dict(N=16, H=64, V=32, d_grad_output=A, grad_X=A, grad_W_acc=A, grad_W=A, grad_b_acc=None,
+                grad_b=None, stream=None)
+    args.update(kw)
+    with pytest.raises(lce.LCEError) as e:
+        lce.lce_scale_grads(*args.values())
+    assert e.value.status == code
+
+
+def test_profile_end_without_begin_is_empty():
+    lce.lce_profile_begin()
+    out = lce.lce_profile_end()
+    assert set(out) == set(lce.PROFILE_KINDS)
+    assert all(v == (0.0, 0) for v in out.values())

@@ -90,3 +90,31 @@ def test_cuda_graph_capture_and_replay():
         torch.cuda.synchronize()
         for k in ("loss", "lse", "gX", "gW", "acc"):
             assert bool((eager[k].view(-1) == g_out[k].view(-1)).all().item()), k
+
+
+def test_profile_counts_launches_per_role():
+    """The per-kernel profiling hook sees one launch of each GEMM role per
+    chunk in the fused call (no recomputed-logits GEMM there), and the
+    recompute GEMM per chunk in lce_backward."""
+    import torch
+    X, W, b, y = random_problem(44, 1000, 128, 4096, bias=False)
+    N, H, V, chunk = 1000, 128, 4096, 256
+    chunks = -(-N // chunk)
+    Xd, Wd, yd = dev_bf16(X), dev_bf16(W), dev_i64(y)
+    o, nws = _buffers(N, H, V, chunk)
+    s = torch.cuda.current_stream()
+    lce.lce_profile_begin()
+    _call(N, H, V, Xd, Wd, yd, chunk, o, nws, s)
+    prof = lce.lce_profile_end()
+    assert prof["logits_lse"][1] == chunks
+    assert prof["recomputed_logits_softmax"][1] == 0
+    assert prof["grad_w"][1] == chunks
+    assert prof["grad_x"][1] in (chunks, 2 * chunks)  # a split product adds its reduction
+    assert all(v[0] > 0 for k, v in prof.items() if v[1] > 0)
+    nws_b = lce.lce_workspace_size(N, H, V, chunk, False, lce.WS_BACKWARD)
+    ws_b = torch.empty(nws_b, dtype=torch.uint8, device="cuda")
+    lce.lce_profile_begin()
+    lce.lce_backward(N, H, V, Xd, Wd, None, yd, -100, chunk, o["lse"], 1.0, None, o["gX"], o["gW"], None,
+                     o["acc"], None, ws_b, nws_b, s)
+    prof = lce.lce_profile_end()
+    assert prof["recomputed_logits_softmax"][1] == chunks and prof["logits_lse"][1] == 0

@@ -27,6 +27,7 @@ import pytest
 import lce_inputs as L
 import lm_head_linear_chunked_gb300 as lce
 import oracle
+from tests import gpu_util
 from tests.gpu_util import BF16_GRAD_TOL, F32_ACC_TOL, LOSS_RTOL, LSE_ATOL, assert_grad, check_against_oracle, \
     host_f64
 
@@ -94,6 +95,7 @@ def test_sampled_rows_and_loss(problem):
     ref = oracle.rows_forward(Xr, Wb, bb, y[rows])
     lse = host_f64(out["lse"])
     err = np.abs(lse[rows] - ref["lse"]).max()
+    gpu_util._record("lse on 512 sampled rows (absolute)", err, LSE_ATOL)
     assert err <= LSE_ATOL, f"lse on sampled rows: max abs err {err}"
     gx_ref = oracle.rows_grad_X(Xr, Wb, bb, y[rows], ref["lse"], s)
     gx = host_f64(out["grad_X"][torch.from_numpy(rows).cuda()])
@@ -104,6 +106,7 @@ def test_sampled_rows_and_loss(problem):
     ok = y != L.IGNORE_INDEX
     expect = (lse[ok].sum() - zt[ok].sum()) / n_valid
     loss = float(out["loss"].item())
+    gpu_util._record("loss identity over all rows (relative)", abs(loss - expect) / abs(expect), LOSS_RTOL)
     assert abs(loss - expect) <= LOSS_RTOL * abs(expect), (loss, expect)
     if w.N <= 16384:
         full = oracle.forward(problem.bits(problem.Xh), Wb, bb, y, block_rows=512, threads=1)
@@ -154,6 +157,7 @@ def test_full_size_accumulation_is_additive(problem):
     ref = acc_whole.double()
     err = float((tot - ref).abs().max().item())
     scale = float(ref.abs().max().item())
+    gpu_util._record("grad_W_acc additivity over row halves", err, F32_ACC_TOL * scale)
     assert err <= F32_ACC_TOL * scale, f"grad_W_acc additivity: {err} > 1e-4 * {scale}"
     if gb_whole is not None:
         tb = parts[0][1].double() + parts[1][1].double()
