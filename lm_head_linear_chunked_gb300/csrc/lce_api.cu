@@ -90,8 +90,8 @@ lce_status_t make_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, bool
     };
     p->off_row_loss = take(fwd, static_cast<size_t>(N) * 4);
     p->off_zt = take(fwd, static_cast<size_t>(p->C) * 4);
-    p->off_pm = take(fwd, static_cast<size_t>(p->n_vt) * p->C * 4);
-    p->off_ps = take(fwd, static_cast<size_t>(p->n_vt) * p->C * 4);
+    p->off_pm = take(fwd, static_cast<size_t>(2 * p->n_vt) * p->C * 4);  // one per 128-column half tile
+    p->off_ps = take(fwd, static_cast<size_t>(2 * p->n_vt) * p->C * 4);
     p->off_g = take(bwd, static_cast<size_t>(p->C) * p->ldg * 2);
     p->off_gb = take(bwd && has_bias, static_cast<size_t>(p->mt_chunk) * 4 * V * 4);
     p->off_keys = take(bwd, static_cast<size_t>(p->n_chunks) * p->label_blocks_per_chunk * LABEL_BLOCK * 8);
@@ -339,7 +339,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.row_map = dmap + r0;
             }
             LCE_LAUNCH(PK_LSE, launch_gemm(MODE_LSE, mX_k, mW_k, a, grid_for(mt * p.n_vt), s));
-            LCE_LAUNCH(PK_OTHER, launch_combine(pm, ps, p.n_vt, p.C, rows, zt, pb.y + r0, pb.ignore_index, o.lse + r0,
+            LCE_LAUNCH(PK_OTHER, launch_combine(pm, ps, 2 * p.n_vt, p.C, rows, zt, pb.y + r0, pb.ignore_index, o.lse + r0,
                                         row_loss + r0, s));
         }
         if (do_bwd) {

@@ -59,12 +59,12 @@ __global__ void scale_kernel(WsHeader* hdr, float grad_scale, const float* d_gra
     if (n_valid_out) *n_valid_out = static_cast<int64_t>(nv);
 }
 
-// lse_i = (M + log2 S) ln 2, where (M, S) merges the vocabulary tiles'
-// partial (max, sum of 2^(t - max)).  Four threads per row each merge every
-// fourth tile in tile order (S <- S 2^(M - M') + s_t 2^(m_t - M') when a
-// larger max m_t = M' arrives, else S <- S + s_t 2^(m_t - M)); the four
-// results are then merged in a fixed order.  Row loss = lse_i - z[i, y_i]
-// for valid rows, else 0.
+// lse_i = (M + log2 S) ln 2, where (M, S) merges the per-half-tile partial
+// (max, sum of 2^(t - max)).  One warp per row: lane k merges partials
+// k, k+32, ... in order (S <- S 2^(M - M') + s_t 2^(m_t - M') when a larger
+// max m_t = M' arrives, else S <- S + s_t 2^(m_t - M)); the 32 results are
+// then merged by a butterfly in a fixed order, so lse does not depend on the
+// chunk size.  Row loss = lse_i - z[i, y_i] for valid rows, else 0.
 __device__ __forceinline__ void merge_partial(float& M, float& S, float m, float s) {
     if (m > M) {
         S = S * exp2f(M - m) + s;
@@ -75,36 +75,35 @@ __device__ __forceinline__ void merge_partial(float& M, float& S, float m, float
 }
 
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
-                                                      int64_t n_vt, int64_t ldp, int64_t rows,
+                                                      int64_t n_pt, int64_t ldp, int64_t rows,
                                                       const float* __restrict__ zt, const int64_t* __restrict__ y,
                                                       int64_t ignore_index, float* __restrict__ lse,
                                                       float* __restrict__ row_loss) {
-    const int g = threadIdx.x & 3;
-    const int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x / 4) + (threadIdx.x >> 2);
+    const int lane = threadIdx.x & 31;
+    const int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
     const bool ok = r < rows;
     float M = -INFINITY, S = 0.f;
     if (ok)
-        for (int64_t t = g; t < n_vt; t += 4) merge_partial(M, S, pm[t * ldp + r], ps[t * ldp + r]);
-    // merge the four groups in a fixed order: (g0 with g1), (g2 with g3), then the two pairs
+        for (int64_t t = lane; t < n_pt; t += 32) merge_partial(M, S, pm[t * ldp + r], ps[t * ldp + r]);
 #pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
+    for (int o = 1; o <= 16; o <<= 1) {
         const float M2 = __shfl_xor_sync(0xFFFFFFFFu, M, o);
         const float S2 = __shfl_xor_sync(0xFFFFFFFFu, S, o);
-        const bool lower = (g & o) == 0;  // both partners merge (lower, upper)
+        const bool lower = (lane & o) == 0;  // both partners merge (lower, upper)
         float Ma = lower ? M : M2, Sa = lower ? S : S2;
         merge_partial(Ma, Sa, lower ? M2 : M, lower ? S2 : S);
         M = Ma;
         S = Sa;
     }
-    if (!ok || g != 0) return;
+    if (!ok || lane != 0) return;
     const float l = (M + log2f(S)) * LN2_F;
     lse[r] = l;
     if (row_loss) row_loss[r] = (y[r] != ignore_index) ? l - zt[r] : 0.f;
 }
 
 // The fused path's softmax without recomputing the logits: the forward
-// stored E = fp16(2^(t - m) 2^15) per (valid row, 256-column vocab tile),
-// with m the tile's max, at the row's compacted position; here, once lse is
+// stored E = fp16(2^(t - m) 2^15) per (valid row, 128-column half of a vocab
+// tile), with m that half tile's max, at the row's compacted position; here, once lse is
 // known, P = fp16(E 2^(m - lse log2 e)) in place (= fp16(p 2^15)).  Compact
 // rows from n_valid up to the next multiple of 64 are zeroed (the K tail of
 // the grad_W product).  One block covers 32 compact rows of one vocab tile:
@@ -139,7 +138,8 @@ __global__ void __launch_bounds__(256) p_rescale_kernel(uint16_t* __restrict__ P
             continue;
         }
         const int64_t r = crow[j];  // chunk row
-        const float f = exp2f(pm[tile * ldp + r] - lse[r] * LOG2E);
+        // the forward kept one max per 128-column half tile
+        const float f = exp2f(pm[(2 * tile + (cg >> 4)) * ldp + r] - lse[r] * LOG2E);
         const uint4 w = *ptr;
         const uint32_t u[4] = {w.x, w.y, w.z, w.w};
         uint32_t o[4];
@@ -660,12 +660,12 @@ cudaError_t launch_scale(WsHeader* hdr, float grad_scale, const float* d_grad_ou
     return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const float* part_m, const float* part_s, int64_t n_vt, int64_t ldp, int64_t rows,
+cudaError_t launch_combine(const float* part_m, const float* part_s, int64_t n_pt, int64_t ldp, int64_t rows,
                            const float* zt, const int64_t* y, int64_t ignore_index, float* lse, float* row_loss,
                            cudaStream_t s) {
-    const int threads = 256;  // 64 rows per block, 4 threads per row
-    const int64_t blocks = (rows + 63) / 64;
-    combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(part_m, part_s, n_vt, ldp, rows, zt, y,
+    const int threads = 256;  // 8 rows per block, one warp per row
+    const int64_t blocks = (rows + 7) / 8;
+    combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(part_m, part_s, n_pt, ldp, rows, zt, y,
                                                                       ignore_index, lse, row_loss);
     return cudaGetLastError();
 }

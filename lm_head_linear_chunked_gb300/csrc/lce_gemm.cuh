@@ -6,9 +6,10 @@
 //   warp 1 (one lane): MMA issuer.  Four tcgen05.mma (M=128, N=256, K=16)
 //          per slice into one of two 256-column fp32 TMEM accumulators;
 //          tcgen05.commit frees ring slots and publishes finished tiles.
-//   warps 2..5: epilogue.  Each thread owns one accumulator row (its TMEM
-//          lane), reads it 32 columns at a time with tcgen05.ld and applies
-//          the role's epilogue while the MMA warp fills the other buffer.
+//   warps 2..9: epilogue.  Each thread owns one accumulator row (its TMEM
+//          lane) and half of its 256 columns, reads them 32 at a time with
+//          tcgen05.ld and applies the role's epilogue while the MMA warp
+//          fills the other buffer.
 //
 // Every wait is bounded (globaltimer); a wait that runs out raises the
 // status bit, flags the CTA to stop, and the CTA drains its in-flight
@@ -192,11 +193,12 @@ __device__ __forceinline__ float warp_column_sums(float (&g)[32], int lane) {
 // zero_acc: the tile had no K work (an empty compacted chunk), so its
 // accumulator reads as zero.
 template <int MODE>
-__device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, int q, int lane,
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, int q, int half, int lane,
                                               uint32_t taddr, uint32_t empty_bar, int64_t m_rows,
                                               bool zero_acc, int ks) {
     const int64_t row = static_cast<int64_t>(m) * BM + q * 32 + lane;
     const int64_t col0 = static_cast<int64_t>(n) * BN;
+    const int j0 = half * (BN / 64);  // this warp's four 32-column chunks: half of the tile's columns
     const bool row_ok = row < m_rows;
     // MODE_LSE / MODE_G: where this row's E or P row goes (-1: not stored)
     const int64_t prow = (a.row_map && row_ok) ? static_cast<int64_t>(a.row_map[row]) : (row_ok ? row : -1);
@@ -210,7 +212,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         float mx = -INFINITY, zt = 0.f;
         bool got = false;
 #pragma unroll 1
-        for (int j = 0; j < BN / 32; ++j) {
+        for (int j = j0; j < j0 + BN / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
             if (c0 >= a.N) break;
             float v[32];
@@ -228,7 +230,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         }
         float sm = 0.f;
 #pragma unroll 1
-        for (int j = 0; j < BN / 32; ++j) {
+        for (int j = j0; j < j0 + BN / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
             if (c0 >= a.N) break;
             float v[32];
@@ -247,8 +249,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar);
         if (row_ok) {
-            a.part_m[static_cast<int64_t>(n) * a.ldp + row] = mx;
-            a.part_s[static_cast<int64_t>(n) * a.ldp + row] = sm;
+            // one partial per 128-column half tile
+            a.part_m[(2 * static_cast<int64_t>(n) + half) * a.ldp + row] = mx;
+            a.part_s[(2 * static_cast<int64_t>(n) + half) * a.ldp + row] = sm;
             if (got) a.zt[row] = zt;
         }
     } else if constexpr (MODE == MODE_G) {
@@ -256,7 +259,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         const bool valid = row_ok && yr != a.ignore_index;
         const float lse2 = row_ok ? a.lse[row] * LOG2E_F : 0.f;
 #pragma unroll 1
-        for (int j = 0; j < BN / 32; ++j) {
+        for (int j = j0; j < j0 + BN / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
             if (c0 >= a.N) break;
             float v[32];
@@ -288,7 +291,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         // by the reduction kernel (fixed slice order)
         float* dst = a.split_out + static_cast<int64_t>(ks) * a.split_stride;
 #pragma unroll 1
-        for (int j = 0; j < BN / 32; ++j) {
+        for (int j = j0; j < j0 + BN / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
             if (c0 >= a.N) break;
             float v[32];
@@ -311,7 +314,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         const bool valid = row_ok && yr != a.ignore_index && yr >= 0 && yr < a.V;
         const uint16_t* wy = a.w_rows + (valid ? yr : 0) * a.ldw;
 #pragma unroll 1
-        for (int j = 0; j < BN / 32; ++j) {
+        for (int j = j0; j < j0 + BN / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
             if (c0 >= a.N) break;
             float v[32];
@@ -338,7 +341,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
     } else if constexpr (MODE == MODE_GRADW) {
         const float s = ldexpf(*a.scale, -(P_SCALE_EXP + operand_scale_exp(*a.b_amax_bits)));
 #pragma unroll 1
-        for (int j = 0; j < BN / 32; ++j) {
+        for (int j = j0; j < j0 + BN / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
             if (c0 >= a.N) break;
             float v[32];
@@ -373,7 +376,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         if (lane == 0) mbar_arrive(empty_bar);
     } else {  // PLAIN: D = fp32 product
 #pragma unroll 1
-        for (int j = 0; j < BN / 32; ++j) {
+        for (int j = j0; j < j0 + BN / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
             if (c0 >= a.N) break;
             float v[32];
@@ -407,7 +410,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctl->tmem_full[b]), 1);
-            mbar_init(smem_u32(&ctl->tmem_empty[b]), 4);
+            mbar_init(smem_u32(&ctl->tmem_empty[b]), EPI_WARPS);
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort_flag = 0;
@@ -540,8 +543,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
         }
     } else {
-        // ---------------- epilogue (warps 2..5; warp w reads TMEM lanes 32*(w%4) ..)
+        // ---------------- epilogue (warps 2..9; warp w reads TMEM lanes 32*(w%4) ..,
+        // warps 2..5 the tile's first 128 columns, warps 6..9 the last 128)
         const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
         uint32_t acc = 0, acc_phase = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             int m, n, ks;
@@ -552,8 +557,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (!wait_phase(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, args.status, limit)) break;
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            epilogue_tile<MODE>(args, m, n, q, lane, taddr, smem_u32(&ctl->tmem_empty[acc]), m_rows, kb1 <= kb0,
-                                ks);
+            epilogue_tile<MODE>(args, m, n, q, half, lane, taddr, smem_u32(&ctl->tmem_empty[acc]), m_rows,
+                                kb1 <= kb0, ks);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }

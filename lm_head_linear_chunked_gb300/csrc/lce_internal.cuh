@@ -34,7 +34,8 @@ constexpr int B_STAGE_BYTES = BN * BK * 2;                 // 32 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES; // 48 KB
 constexpr int CTL_BYTES = 256;
 constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + CTL_BYTES;
-constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int EPI_WARPS = 8;        // two per TMEM lane quarter, one per 128-column half
+constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
 constexpr uint32_t TMEM_COLS = 512; // two 256-column fp32 accumulators
 
 // Device status word bits (bit k set = lce_status_t k was raised).
@@ -91,8 +92,8 @@ struct GemmArgs {
     const int64_t* y;  // labels of this chunk's first row
     int64_t ignore_index;
     const uint16_t* bias;  // nullable
-    float* part_m;     // [n_tiles, ldp] per-row running max (base-2 units)
-    float* part_s;     // [n_tiles, ldp] per-row sum of 2^(t - max)
+    float* part_m;     // [2 n_tiles, ldp] per-row max of each 128-column half tile (base-2 units)
+    float* part_s;     // [2 n_tiles, ldp] per-row sum of 2^(t - max) over the half tile
     float* zt;         // [chunk rows] target logit
     int64_t ldp;
     const float* lse;  // this chunk's first row
