@@ -27,6 +27,7 @@ processed divided by the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -46,11 +47,24 @@ WORKLOAD = "qwen3-8b-head-N131072-H4096-V151936"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 # DRAM bytes (read + write) of one full-size launch of each GEMM role on this
 # workload, from the ncu capture summarised in
-# profiles/gemm_dram_full_qwen3-8b-head.md.  None once a kernel has changed
-# since its counters were taken.
-DRAM_BYTES_PER_LAUNCH = {"grad_w": 23.07e9 + 2.47e9, "grad_x": 23.25e9 + 0.13e9,
-                         "logits_lse": 5.17e9 + 4.78e9, "recomputed_logits_softmax": None}
+# profiles/gemm_dram_full_qwen3-8b-head.md.  They hold only for the sources
+# they were captured with: DRAM_BYTES_SOURCES lists the files that decide a
+# GEMM launch's traffic and DRAM_BYTES_DIGEST their SHA-256 at capture time.
+# When the digest no longer matches, roofline.traffic is reported as null.
+DRAM_BYTES_PER_LAUNCH = {"grad_w": 25.57e9 + 2.47e9, "grad_x": 31.70e9 + 0.13e9,
+                         "logits_lse": 5.21e9 + 4.87e9, "recomputed_logits_softmax": None}
 DRAM_BYTES_CHUNK_ROWS = 16384  # the chunk size those launches ran with
+DRAM_BYTES_SOURCES = ["csrc/lce_gemm.cuh", "csrc/lce_internal.cuh", "csrc/lce_ptx.cuh", "csrc/lce_api.cu",
+                      "csrc/lce_gemm_logits.cu", "csrc/lce_gemm_grads.cu"]
+DRAM_BYTES_DIGEST = "5a4a9d574f319420"
+
+
+def gemm_source_digest() -> str:
+    h = hashlib.sha256()
+    for rel in DRAM_BYTES_SOURCES:
+        with open(os.path.join(ROOT, "lm_head_linear_chunked_gb300", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def load_peaks():
@@ -452,7 +466,9 @@ def run_ours(args, w):
         "roofline": {"bound": "tensor", "achieved": dom_tflops, "peak": sustained, "unit": "TFLOP/s",
                      "frac": dom_tflops / sustained,
                      "traffic": DRAM_BYTES_PER_LAUNCH.get(dom) if args.workload == WORKLOAD and not args.shape
-                     and C == DRAM_BYTES_CHUNK_ROWS else None,
+                     and C == DRAM_BYTES_CHUNK_ROWS and gemm_source_digest() == DRAM_BYTES_DIGEST else None,
+                     "traffic_source": f"ncu capture of sources {DRAM_BYTES_DIGEST}; these sources "
+                                       f"{gemm_source_digest()}",
                      "kernel": f"gemm_kernel ({dom})",
                      "flops_per_launch": dom_flops_per_launch, "launches": dom_n,
                      "mean_launch_ms": dom_ms / dom_n,

@@ -195,7 +195,7 @@ __device__ __forceinline__ float warp_column_sums(float (&g)[32], int lane) {
 template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, int q, int half, int lane,
                                               uint32_t taddr, uint32_t empty_bar, int64_t m_rows,
-                                              bool zero_acc, int ks) {
+                                              bool zero_acc, int ks, const float4 (&pre)[8]) {
     const int64_t row = static_cast<int64_t>(m) * BM + q * 32 + lane;
     const int64_t col0 = static_cast<int64_t>(n) * BN;
     const int j0 = half * (BN / 64);  // this warp's four 32-column chunks: half of the tile's columns
@@ -339,36 +339,55 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         if (lane == 0) mbar_arrive(empty_bar);
       }
     } else if constexpr (MODE == MODE_GRADW) {
+        // grad_W_acc[v, h] (+)= s * acc.  The accumulator's old values are
+        // read one 32-column chunk ahead (the first chunk by the caller,
+        // before the tile's MMAs finished), so the read latency of the
+        // read-modify-write overlaps the previous chunk's work.
         const float s = ldexpf(*a.scale, -(P_SCALE_EXP + operand_scale_exp(*a.b_amax_bits)));
-#pragma unroll 1
-        for (int j = j0; j < j0 + BN / 64; ++j) {
+        const bool rmw = row_ok && !a.acc_first;
+        float4 cur[8];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) cur[g] = pre[g];
+#pragma unroll
+        for (int jj = 0; jj < BN / 64; ++jj) {
+            const int j = j0 + jj;
             const int64_t c0 = col0 + 32 * j;
-            if (c0 >= a.N) break;
-            float v[32];
-            tmem_load_32cols(taddr + 32 * j, v);
-            if (zero_acc) {
+            if (c0 < a.N) {
+                float4 nxt[8];
+                const bool more = rmw && jj + 1 < BN / 64 && c0 + 32 < a.N;
+                if (more) {
+                    const float* p1 = a.out_f32 + row * a.ld_f32 + c0 + 32;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0.f;
-            }
-            if (row_ok) {
-                float* p = a.out_f32 + row * a.ld_f32 + c0;
-                if (a.acc_first) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= s;
+                    for (int g = 0; g < 8; ++g) nxt[g] = *reinterpret_cast<const float4*>(p1 + 4 * g);
                 } else {
-                    float4 old[8];
 #pragma unroll
-                    for (int g = 0; g < 8; ++g) old[g] = *reinterpret_cast<const float4*>(p + 4 * g);
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        v[4 * g + 0] = fmaf(s, v[4 * g + 0], old[g].x);
-                        v[4 * g + 1] = fmaf(s, v[4 * g + 1], old[g].y);
-                        v[4 * g + 2] = fmaf(s, v[4 * g + 2], old[g].z);
-                        v[4 * g + 3] = fmaf(s, v[4 * g + 3], old[g].w);
-                    }
+                    for (int g = 0; g < 8; ++g) nxt[g] = cur[g];
                 }
-                store_f32_32(p, v, 32);
-                if (a.write_bf16) store_bf16_32(a.out_bf16 + row * a.ld_out + c0, v, 32);
+                float v[32];
+                tmem_load_32cols(taddr + 32 * j, v);
+                if (zero_acc) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                }
+                if (row_ok) {
+                    if (a.acc_first) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] *= s;
+                    } else {
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            v[4 * g + 0] = fmaf(s, v[4 * g + 0], cur[g].x);
+                            v[4 * g + 1] = fmaf(s, v[4 * g + 1], cur[g].y);
+                            v[4 * g + 2] = fmaf(s, v[4 * g + 2], cur[g].z);
+                            v[4 * g + 3] = fmaf(s, v[4 * g + 3], cur[g].w);
+                        }
+                    }
+                    float* p = a.out_f32 + row * a.ld_f32 + c0;
+                    store_f32_32(p, v, 32);
+                    if (a.write_bf16) store_bf16_32(a.out_bf16 + row * a.ld_out + c0, v, 32);
+                }
+#pragma unroll
+                for (int g = 0; g < 8; ++g) cur[g] = nxt[g];
             }
         }
         tc_fence_before_sync();
@@ -554,11 +573,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (static_cast<int64_t>(m) * BM >= m_rows) continue;
             const int kb0 = args.k_splits > 1 ? ks * args.k_per_split : 0;
             const int kb1 = args.k_splits > 1 ? min(k_blocks, kb0 + args.k_per_split) : k_blocks;
+            float4 pre[8];
+            if constexpr (MODE == MODE_GRADW) {
+                // first chunk of the accumulator's old values, read before the tile's MMAs finish
+                const int64_t row = static_cast<int64_t>(m) * BM + q * 32 + lane;
+                const int64_t c0 = static_cast<int64_t>(n) * BN + 128 * half;
+                if (!args.acc_first && row < m_rows && c0 < args.N) {
+                    const float* p0 = args.out_f32 + row * args.ld_f32 + c0;
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) pre[g] = *reinterpret_cast<const float4*>(p0 + 4 * g);
+                } else {
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) pre[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
             if (!wait_phase(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, args.status, limit)) break;
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             epilogue_tile<MODE>(args, m, n, q, half, lane, taddr, smem_u32(&ctl->tmem_empty[acc]), m_rows,
-                                kb1 <= kb0, ks);
+                                kb1 <= kb0, ks, pre);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
