@@ -248,6 +248,10 @@ def run_ours(args, w):
     ws_n, rank, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    prev_form = lce.lce_set_gemm_form(args.gemm_form or "single")
+    if not args.gemm_form:
+        lce.lce_set_gemm_form(prev_form)  # keep the library's default
+    gemm_form = args.gemm_form or {lce.GEMM_SINGLE: "single", lce.GEMM_PAIR: "pair"}[prev_form]
     if ws_n > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
@@ -453,6 +457,7 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": 1e3 * t_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "N": N, "H": H, "V": V, "chunk_rows": C, "chunks": n_chunks,
+                   "gemm_form": gemm_form,
                    "bias": False, "ignored_rows": int((yh == -100).sum().item()),
                    "l2": f"inputs larger than L2 (X {N * H * 2 / 1e9:.2f} GB, W {V * H * 2 / 1e9:.2f} GB; L2 129 MB)",
                    "parallelism": "replicas" if ws_n > 1 else "single GPU"},
@@ -497,6 +502,8 @@ def run_gemm(args):
     import __graft_entry__
     import lm_head_linear_chunked_gb300 as lce
     __graft_entry__.build()
+    if args.gemm_form:
+        lce.lce_set_gemm_form(args.gemm_form)
     M, N, K, layout = (int(x) for x in args.gemm.split(","))
     torch.manual_seed(0)
     a_shape = (M, K) if layout in (0, 1) else (K, M)
@@ -532,6 +539,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=256, help="rows of the CPU-oracle baseline sample")
     ap.add_argument("--ref-rows", type=int, default=32, help="rows per step of --impl reference")
     ap.add_argument("--gemm", default=None, help="M,N,K,layout: time the bare GEMM core instead")
+    ap.add_argument("--gemm-form", choices=["single", "pair"], default=None,
+                    help="tensor-core GEMM form (default: the library's)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-split", action="store_true", help="skip timing lce_forward and lce_backward alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -214,6 +214,30 @@ LCE_API lce_status_t lce_forward_static_ws(int64_t N, int64_t H, int64_t V,
                                    float* loss, float* lse, int64_t* n_valid,
                                    lce_stream_t stream);
 
+/* lce_set_gemm_form: the tensor-core GEMM form of the calls this process
+ * makes after it (each call reads the setting once, when it is made).
+ *   LCE_GEMM_SINGLE: one CTA per SM computes 128x256 output tiles with
+ *     tcgen05.mma cta_group::1 and a 4-stage ring of 48 KB slices.
+ *   LCE_GEMM_PAIR: a cluster of two CTAs on neighbouring SMs computes
+ *     256x256 tiles with one tcgen05.mma of M = 256 (cta_group::2); each
+ *     SM loads its own half of B, so a 64-wide K slice brings 32 KB into
+ *     each SM instead of 48 KB, and the ring is 6 stages deep.  On a device
+ *     that cannot keep any cluster of two resident, calls use SINGLE.
+ * The products are the ones the documentation of each entry point states
+ * in either form.  The forms may differ in the last bits of FP32 sums;
+ * each form is deterministic.  The workspace does not depend on the form.
+ * Returns the previous form, or -1 for an unknown value (nothing changes).
+ * Host-only; safe to call from any thread. */
+#define LCE_GEMM_SINGLE 0
+#define LCE_GEMM_PAIR 1
+LCE_API int lce_set_gemm_form(int form);
+
+/* lce_gemm_pair_slots: how many CTA pairs of the pair form the current
+ * device keeps resident at once (one per two SMs when every pair fits);
+ * 0 when the pair form cannot run there (calls then use SINGLE) or no
+ * device is usable. */
+LCE_API int lce_gemm_pair_slots(void);
+
 /* Per-kernel device time, for benchmarks.  Between lce_profile_begin() and
  * lce_profile_end(), every kernel the library enqueues is bracketed by two
  * CUDA events recorded on the call's own stream (events are created on

@@ -58,6 +58,8 @@ _SIGS = {
     "lce_debug_wait_timeout": [ctypes.c_uint32, _P, ctypes.c_size_t, _P],
     "lce_forward_static_ws": [_I64, _I64, _I64, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _P],
     "lce_scale_grads": [_I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P],
+    "lce_set_gemm_form": [ctypes.c_int],
+    "lce_gemm_pair_slots": [],
     "lce_profile_begin": [],
     "lce_profile_end": [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64)],
 }
@@ -83,7 +85,8 @@ def lib() -> ctypes.CDLL:
             for name, argtypes in _SIGS.items():
                 f = getattr(L, name)
                 f.argtypes = argtypes
-                f.restype = ctypes.c_char_p if name == "lce_status_string" else _STATUS
+                f.restype = (ctypes.c_char_p if name == "lce_status_string" else
+                             ctypes.c_int if name in ("lce_set_gemm_form", "lce_gemm_pair_slots") else _STATUS)
             _lib = L
     return _lib
 
@@ -181,6 +184,24 @@ def lce_debug_gemm(layout, M, N, K, A, B, D, ws, ws_bytes, stream) -> None:
 
 def lce_debug_wait_timeout(limit_us, ws, ws_bytes, stream) -> None:
     _check(lib().lce_debug_wait_timeout(limit_us, _ptr(ws), ws_bytes, _stream(stream)), "lce_debug_wait_timeout")
+
+
+GEMM_SINGLE, GEMM_PAIR = 0, 1
+GEMM_FORMS = {"single": GEMM_SINGLE, "pair": GEMM_PAIR}
+
+
+def lce_set_gemm_form(form) -> int:
+    """Selects the GEMM form of later calls ("single"/0 or "pair"/1); returns the previous one."""
+    f = GEMM_FORMS.get(form, form)
+    prev = lib().lce_set_gemm_form(int(f))
+    if prev < 0:
+        raise ValueError(f"unknown GEMM form {form!r}")
+    return prev
+
+
+def lce_gemm_pair_slots() -> int:
+    """CTA pairs of the pair form resident at once on the current device (0: not available)."""
+    return int(lib().lce_gemm_pair_slots())
 
 
 def lce_profile_begin() -> None:

@@ -17,10 +17,11 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 constexpr int64_t AUTO_CHUNK_ROWS = 16384;
-// Tile-order groups: 32 row tiles of X (4096 rows, 32 MB at H = 4096) for
-// the logits passes; for the grad_W pass, as many 256-column tiles of the
+// Tile-order groups: 4096 rows of X (32 MB at H = 4096) for the logits
+// passes, 2048 rows of P for grad_X; for the grad_W pass, as many 256-column tiles of the
 // fp16 X chunk as make about 32 MB (8 at 8192 rows, 4 at 16384).
-constexpr int32_t LOGITS_GROUP_M = 32;
+constexpr int64_t LOGITS_GROUP_ROWS = 4096;
+constexpr int64_t GRADX_GROUP_ROWS = 2048;
 constexpr int64_t GROUP_BYTES = 32ll << 20;
 
 // grad_X of a chunk with few output tiles (e.g. 256-row chunks) is split
@@ -157,10 +158,28 @@ int sm_count() {
     return n;
 }
 
-int grid_for(int64_t tiles) {
-    const int sms = sm_count();
-    if (sms <= 0) return 0;
-    return static_cast<int>(tiles < sms ? tiles : sms);
+// The GEMM form of this process's calls (lce_set_gemm_form), read once per call.
+std::atomic<int> g_gemm_form{LCE_GEMM_SINGLE};
+
+struct Form {
+    bool pair;
+    int64_t rows;  // output rows per tile: 128, or 256 shared by a pair
+    int slots;     // tiles in flight at once: SMs, or resident pairs
+};
+
+Form gemm_form() {
+    Form f;
+    f.pair = g_gemm_form.load(std::memory_order_relaxed) == LCE_GEMM_PAIR && gemm_pair_slots() > 0;
+    f.rows = f.pair ? PAIR_BM : BM;
+    f.slots = f.pair ? gemm_pair_slots() : sm_count();
+    return f;
+}
+
+// Grid of a persistent GEMM launch over `units` tiles (x K slices).
+int grid_of(const Form& f, int64_t units) {
+    if (f.slots <= 0) return 0;
+    const int64_t n = units < f.slots ? units : f.slots;
+    return static_cast<int>(f.pair ? 2 * n : n);
 }
 
 GemmArgs base_args(WsHeader* hdr) {
@@ -268,6 +287,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     }
     if (ws_bytes < p.total) return LCE_ERR_WORKSPACE;
     if (!encode_fn() || sm_count() <= 0) return LCE_ERR_CUDA;
+    const Form form = gemm_form();
 
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     WsHeader* hdr = reinterpret_cast<WsHeader*>(wsb);
@@ -290,7 +310,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
 
     // operand maps of the whole X and W
     CUtensorMap mX_k, mW_k, mW16_mn;
-    if (!map_16bit_2d(&mX_k, pb.X, pb.N, pb.H, pb.H, 64, BM) || !map_16bit_2d(&mW_k, pb.W, pb.V, pb.H, pb.H, 64, BN))
+    if (!map_16bit_2d(&mX_k, pb.X, pb.N, pb.H, pb.H, 64, BM) || !map_16bit_2d(&mW_k, pb.W, pb.V, pb.H, pb.H, 64, B_BOX_ROWS))
         return LCE_ERR_CUDA;
     if (do_bwd && !map_16bit_2d(&mW16_mn, W16, pb.V, pb.H, pb.H, 64, 64, true)) return LCE_ERR_CUDA;
 
@@ -315,14 +335,15 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     for (int64_t c = 0; c < p.n_chunks; ++c) {
         const int64_t r0 = c * p.C;
         const int64_t rows = (pb.N - r0) < p.C ? (pb.N - r0) : p.C;
-        const int64_t mt = cdiv(rows, BM);
+        const int64_t mt = cdiv(rows, BM);        // 128-row tiles (grad_b partial rows)
+        const int64_t mtf = cdiv(rows, form.rows);  // tiles of the GEMM form
         if (do_fwd) {
             GemmArgs a = base_args(hdr);
-            a.m_tiles = static_cast<int32_t>(mt);
+            a.m_tiles = static_cast<int32_t>(mtf);
             a.n_tiles = static_cast<int32_t>(p.n_vt);
             a.k_blocks = static_cast<int32_t>(cdiv(pb.H, BK));
             a.raster = 2;
-            a.group_m = LOGITS_GROUP_M;
+            a.group_m = static_cast<int32_t>(LOGITS_GROUP_ROWS / form.rows);
             a.a_y0 = static_cast<int32_t>(r0);
             a.M = rows;
             a.N = pb.V;
@@ -338,7 +359,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.ldg = p.ldg;
                 a.row_map = dmap + r0;
             }
-            LCE_LAUNCH(PK_LSE, launch_gemm(MODE_LSE, mX_k, mW_k, a, grid_for(mt * p.n_vt), s));
+            LCE_LAUNCH(PK_LSE, launch_gemm(MODE_LSE, mX_k, mW_k, a, grid_of(form, mtf * p.n_vt), s, form.pair));
             LCE_LAUNCH(PK_OTHER, launch_combine(pm, ps, 2 * p.n_vt, p.C, rows, zt, pb.y + r0, pb.ignore_index, o.lse + r0,
                                         row_loss + r0, s));
         }
@@ -349,11 +370,11 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                                                       gb, s));
             } else {   // recompute the logits; P = softmax (fp16)
                 GemmArgs a = base_args(hdr);
-                a.m_tiles = static_cast<int32_t>(mt);
+                a.m_tiles = static_cast<int32_t>(mtf);
                 a.n_tiles = static_cast<int32_t>(p.n_vt);
                 a.k_blocks = static_cast<int32_t>(cdiv(pb.H, BK));
                 a.raster = 2;
-                a.group_m = LOGITS_GROUP_M;
+                a.group_m = static_cast<int32_t>(LOGITS_GROUP_ROWS / form.rows);
                 a.a_y0 = static_cast<int32_t>(r0);
                 a.M = rows;
                 a.N = pb.V;
@@ -365,7 +386,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.ldg = p.ldg;
                 a.gb_part = gb;
                 a.row_map = dmap + r0;
-                LCE_LAUNCH(PK_P, launch_gemm(MODE_G, mX_k, mW_k, a, grid_for(mt * p.n_vt), s));
+                LCE_LAUNCH(PK_P, launch_gemm(MODE_G, mX_k, mW_k, a, grid_of(form, mtf * p.n_vt), s, form.pair));
             }
             if (gb)
                 LCE_LAUNCH(PK_OTHER, launch_grad_b(gb, mt * 4, pb.V, hdr, counts, o.grad_b_acc, o.grad_b, first, last, s));
@@ -379,11 +400,11 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 return LCE_ERR_CUDA;
             if (o.grad_X) {   // grad_X_c = s (P W - W[y])
                 GemmArgs a = base_args(hdr);
-                a.m_tiles = static_cast<int32_t>(mt);
+                a.m_tiles = static_cast<int32_t>(mtf);
                 a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
                 a.k_blocks = static_cast<int32_t>(cdiv(pb.V, BK));
                 a.raster = 2;
-                a.group_m = 16;
+                a.group_m = static_cast<int32_t>(GRADX_GROUP_ROWS / form.rows);
                 a.M = rows;
                 a.N = pb.H;
                 a.scale = &hdr->scale;
@@ -402,8 +423,9 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.split_out = split_out;
                 a.split_stride = p.C * pb.H;
                 LCE_LAUNCH(PK_GRADX, launch_gemm(MODE_GRADX, mG_k, mW16_mn, a,
-                                                 grid_for(static_cast<int64_t>(a.m_tiles) * a.n_tiles * p.gradx_splits),
-                                                 s));
+                                                 grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles *
+                                                                   p.gradx_splits),
+                                                 s, form.pair));
                 if (split_out)
                     LCE_LAUNCH(PK_GRADX, launch_gradx_split_reduce(split_out, p.gradx_splits, p.C * pb.H, pb.H, crow + r0,
                                                                    nvc + c, rows, pb.y + r0, pb.ignore_index, pb.V,
@@ -411,7 +433,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             }
             {   // grad_W_acc (+)= s P^T X_c
                 GemmArgs a = base_args(hdr);
-                a.m_tiles = static_cast<int32_t>(cdiv(pb.V, BM));
+                a.m_tiles = static_cast<int32_t>(cdiv(pb.V, form.rows));
                 a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
                 a.k_blocks = static_cast<int32_t>(cdiv(rows, BK));
                 a.raster = 3;
@@ -427,7 +449,9 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.write_bf16 = last && o.grad_W != nullptr;
                 a.b_amax_bits = &hdr->amax_x_bits;
                 a.dyn_rows = nvc + c;
-                LCE_LAUNCH(PK_GRADW, launch_gemm(MODE_GRADW, mG_mn, mX16_mn, a, grid_for(static_cast<int64_t>(a.m_tiles) * a.n_tiles), s));
+                LCE_LAUNCH(PK_GRADW, launch_gemm(MODE_GRADW, mG_mn, mX16_mn, a,
+                                                 grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles), s,
+                                                 form.pair));
             }
             // grad_W_acc[y_i] -= s X[i] for the chunk's valid rows, exactly, in row order
             for (int64_t k = 0; k < p.label_blocks_per_chunk; ++k) {
@@ -446,14 +470,14 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
 }  // namespace
 
 cudaError_t launch_gemm(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
-                        int grid, cudaStream_t stream) {
+                        int grid, cudaStream_t stream, bool pair) {
     if (grid <= 0) return cudaErrorInvalidConfiguration;
     switch (mode) {
         case MODE_LSE:
-        case MODE_G: return launch_gemm_logits(mode, map_a, map_b, args, grid, stream);
+        case MODE_G: return launch_gemm_logits(mode, map_a, map_b, args, grid, stream, pair);
         case MODE_GRADX:
-        case MODE_GRADW: return launch_gemm_grads(mode, map_a, map_b, args, grid, stream);
-        default: return launch_gemm_plain(mode, map_a, map_b, args, grid, stream);
+        case MODE_GRADW: return launch_gemm_grads(mode, map_a, map_b, args, grid, stream, pair);
+        default: return launch_gemm_plain(mode, map_a, map_b, args, grid, stream, pair);
     }
 }
 
@@ -610,14 +634,15 @@ lce_status_t lce_debug_gemm(int layout, int64_t M, int64_t N, int64_t K, const l
     CUtensorMap ma, mb;
     bool ok;
     if (layout == 0)
-        ok = map_16bit_2d(&ma, A, M, K, K, 64, BM) && map_16bit_2d(&mb, B, N, K, K, 64, BN);
+        ok = map_16bit_2d(&ma, A, M, K, K, 64, BM) && map_16bit_2d(&mb, B, N, K, K, 64, B_BOX_ROWS);
     else if (layout == 1)
         ok = map_16bit_2d(&ma, A, M, K, K, 64, BM) && map_16bit_2d(&mb, B, K, N, N, 64, 64);
     else
         ok = map_16bit_2d(&ma, A, K, M, M, 64, 64) && map_16bit_2d(&mb, B, K, N, N, 64, 64);
     if (!ok) return LCE_ERR_CUDA;
+    const Form form = gemm_form();
     GemmArgs a = base_args(hdr);
-    a.m_tiles = static_cast<int32_t>(cdiv(M, BM));
+    a.m_tiles = static_cast<int32_t>(cdiv(M, form.rows));
     a.n_tiles = static_cast<int32_t>(cdiv(N, BN));
     a.k_blocks = static_cast<int32_t>(cdiv(K, BK));
     a.raster = 0;
@@ -626,8 +651,16 @@ lce_status_t lce_debug_gemm(int layout, int64_t M, int64_t N, int64_t K, const l
     a.out_f32 = D;
     a.ld_f32 = N;
     LCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
-    LCE_TRY_CUDA(launch_gemm(layout, ma, mb, a, grid_for(static_cast<int64_t>(a.m_tiles) * a.n_tiles), s));
+    LCE_TRY_CUDA(launch_gemm(layout, ma, mb, a, grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles), s,
+                             form.pair));
     return LCE_OK;
+}
+
+int lce_gemm_pair_slots(void) { return gemm_pair_slots(); }
+
+int lce_set_gemm_form(int form) {
+    if (form != LCE_GEMM_SINGLE && form != LCE_GEMM_PAIR) return -1;
+    return g_gemm_form.exchange(form);
 }
 
 lce_status_t lce_debug_wait_timeout(uint32_t limit_us, void* ws, size_t ws_bytes, lce_stream_t stream) {

@@ -189,13 +189,37 @@ __device__ __forceinline__ float warp_column_sums(float (&g)[32], int lane) {
     return g[0];
 }
 
+// The FP32 grad_W accumulator values a warp's lane reads for the 32x32 block
+// at rows row_base .. +31, columns c0 .. c0+31: rows (lane >> 3) + 4i
+// (i = 0..7), columns c0 + 4 (lane & 7) .. +3; rows past m_rows read as 0.
+__device__ __forceinline__ void gradw_load_old(const GemmArgs& a, int64_t row_base, int64_t m_rows, int64_t c0,
+                                               int lane, float4 (&o)[8]) {
+    const float* p = a.out_f32 + c0 + 4 * (lane & 7);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t r = row_base + (lane >> 3) + 4 * i;
+        o[i] = r < m_rows ? *reinterpret_cast<const float4*>(p + r * a.ld_f32) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// Hands an accumulator back to the MMA issuer once a warp has read it: a
+// local arrive, or in the pair form an arrive on rank 0's barrier (given by
+// its cluster address).
+template <bool PAIR>
+__device__ __forceinline__ void release_acc(uint32_t bar) {
+    if constexpr (PAIR)
+        mbar_arrive_cluster(bar);
+    else
+        mbar_arrive(bar);
+}
+
 // m_rows: rows of the output that exist (a.M, or the compacted row count);
 // zero_acc: the tile had no K work (an empty compacted chunk), so its
 // accumulator reads as zero.
-template <int MODE>
+template <int MODE, bool PAIR = false>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, int q, int half, int lane,
                                               uint32_t taddr, uint32_t empty_bar, int64_t m_rows,
-                                              bool zero_acc, int ks, const float4 (&pre)[8]) {
+                                              bool zero_acc, int ks, const float4 (&pre)[8], float* stage) {
     const int64_t row = static_cast<int64_t>(m) * BM + q * 32 + lane;
     const int64_t col0 = static_cast<int64_t>(n) * BN;
     const int j0 = half * (BN / 64);  // this warp's four 32-column chunks: half of the tile's columns
@@ -247,7 +271,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar);
+        if (lane == 0) release_acc<PAIR>(empty_bar);
         if (row_ok) {
             // one partial per 128-column half tile
             a.part_m[(2 * static_cast<int64_t>(n) + half) * a.ldp + row] = mx;
@@ -277,14 +301,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
                 for (int i = 0; i < 32; ++i) ps[i] = v[i] * P_SCALE;
                 store_f16_32(a.g + prow * a.ldg + c0, ps, static_cast<int>(min64(32, a.ldg - c0)));
             }
-            if (a.gb_part) {
+            if (a.gb_part && static_cast<int64_t>(m) * BM < a.M) {  // (a pair's second tile may lie past M)
                 const float cs = warp_column_sums(v, lane);
                 if (c0 + lane < a.N) a.gb_part[(static_cast<int64_t>(m) * 4 + q) * a.N + c0 + lane] = cs;
             }
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar);
+        if (lane == 0) release_acc<PAIR>(empty_bar);
     } else if constexpr (MODE == MODE_GRADX) {
       if (a.k_splits > 1) {
         // one K slice of a split product: the raw fp32 partial sums, finished
@@ -304,7 +328,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar);
+        if (lane == 0) release_acc<PAIR>(empty_bar);
       } else {
         // grad_X[i] = s (sum_v P[i,v] W[v] - W[y_i]); P rows of ignored rows are 0
         const float s = *a.scale;
@@ -336,63 +360,73 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar);
+        if (lane == 0) release_acc<PAIR>(empty_bar);
       }
     } else if constexpr (MODE == MODE_GRADW) {
-        // grad_W_acc[v, h] (+)= s * acc.  The accumulator's old values are
-        // read one 32-column chunk ahead (the first chunk by the caller,
-        // before the tile's MMAs finished), so the read latency of the
-        // read-modify-write overlaps the previous chunk's work.
+        // grad_W_acc[v, h] (+)= s * acc.  Each 32x32 block (the warp's 32
+        // rows, 32 columns) goes through the warp's shared-memory buffer, so
+        // that the accumulator is read and written a whole 128-byte row
+        // segment per 8 lanes (4 rows per instruction) instead of 16 bytes
+        // of 32 different rows.  The old values are read one block ahead
+        // (the first block by the caller, before the tile's MMAs finished).
         const float s = ldexpf(*a.scale, -(P_SCALE_EXP + operand_scale_exp(*a.b_amax_bits)));
-        const bool rmw = row_ok && !a.acc_first;
+        const int64_t row_base = static_cast<int64_t>(m) * BM + q * 32;
+        const int g = lane & 7;
         float4 cur[8];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) cur[g] = pre[g];
+        for (int i = 0; i < 8; ++i) cur[i] = pre[i];
 #pragma unroll
         for (int jj = 0; jj < BN / 64; ++jj) {
             const int j = j0 + jj;
             const int64_t c0 = col0 + 32 * j;
             if (c0 < a.N) {
-                float4 nxt[8];
-                const bool more = rmw && jj + 1 < BN / 64 && c0 + 32 < a.N;
-                if (more) {
-                    const float* p1 = a.out_f32 + row * a.ld_f32 + c0 + 32;
+                {
+                    float v[32];
+                    tmem_load_32cols(taddr + 32 * j, v);
+                    if (zero_acc) {
 #pragma unroll
-                    for (int g = 0; g < 8; ++g) nxt[g] = *reinterpret_cast<const float4*>(p1 + 4 * g);
-                } else {
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) nxt[g] = cur[g];
-                }
-                float v[32];
-                tmem_load_32cols(taddr + 32 * j, v);
-                if (zero_acc) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
-                }
-                if (row_ok) {
-                    if (a.acc_first) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] *= s;
-                    } else {
-#pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            v[4 * g + 0] = fmaf(s, v[4 * g + 0], cur[g].x);
-                            v[4 * g + 1] = fmaf(s, v[4 * g + 1], cur[g].y);
-                            v[4 * g + 2] = fmaf(s, v[4 * g + 2], cur[g].z);
-                            v[4 * g + 3] = fmaf(s, v[4 * g + 3], cur[g].w);
-                        }
+                        for (int i = 0; i < 32; ++i) v[i] = 0.f;
                     }
-                    float* p = a.out_f32 + row * a.ld_f32 + c0;
-                    store_f32_32(p, v, 32);
-                    if (a.write_bf16) store_bf16_32(a.out_bf16 + row * a.ld_out + c0, v, 32);
-                }
+                    // lane = row: 16-byte slot k of the row at slot k ^ (row & 7)
 #pragma unroll
-                for (int g = 0; g < 8; ++g) cur[g] = nxt[g];
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<float4*>(stage + lane * 32 + ((k ^ (lane & 7)) << 2)) =
+                            make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                }
+                __syncwarp();
+                float4 nxt[8];
+                if (!a.acc_first && jj + 1 < BN / 64 && c0 + 32 < a.N)
+                    gradw_load_old(a, row_base, m_rows, c0 + 32, lane, nxt);
+                else
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) nxt[i] = cur[i];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int rr = (lane >> 3) + 4 * i;
+                    const float4 x = *reinterpret_cast<const float4*>(stage + rr * 32 + ((g ^ (rr & 7)) << 2));
+                    const int64_t r = row_base + rr;
+                    if (r < m_rows) {
+                        float4 o;
+                        if (a.acc_first) {
+                            o = make_float4(s * x.x, s * x.y, s * x.z, s * x.w);
+                        } else {
+                            o = make_float4(fmaf(s, x.x, cur[i].x), fmaf(s, x.y, cur[i].y), fmaf(s, x.z, cur[i].z),
+                                            fmaf(s, x.w, cur[i].w));
+                        }
+                        *reinterpret_cast<float4*>(a.out_f32 + r * a.ld_f32 + c0 + 4 * g) = o;
+                        if (a.write_bf16)
+                            *reinterpret_cast<uint2*>(a.out_bf16 + r * a.ld_out + c0 + 4 * g) =
+                                make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+                    }
+                }
+                __syncwarp();  // the buffer is rewritten by the next block
+#pragma unroll
+                for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
             }
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar);
+        if (lane == 0) release_acc<PAIR>(empty_bar);
     } else {  // PLAIN: D = fp32 product
 #pragma unroll 1
         for (int j = j0; j < j0 + BN / 64; ++j) {
@@ -404,7 +438,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar);
+        if (lane == 0) release_acc<PAIR>(empty_bar);
     }
 }
 
@@ -421,6 +455,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint64_t limit = args.timeout_ns;
+    // grad_W epilogue: this warp's block buffer (launched with the extra bytes)
+    float* const epi_stage = reinterpret_cast<float*>(smem_raw + (base - raw) + STAGES * STAGE_BYTES + CTL_BYTES) +
+                             (warp >= 2 ? (warp - 2) * EPI_STAGE_FLOATS : 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -485,7 +522,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             tma_load_2d(sa + j * 8192, &map_a, fb, m * BM + 64 * j, args.a_y0 + k0);
                     }
                     if constexpr (!T::B_MN) {
-                        tma_load_2d(sb, &map_b, fb, k0, args.b_y0 + n * BN);
+#pragma unroll
+                        for (int j = 0; j < BN / B_BOX_ROWS; ++j)
+                            tma_load_2d(sb + j * (B_BOX_ROWS * 128), &map_b, fb, k0,
+                                        args.b_y0 + n * BN + B_BOX_ROWS * j);
                     } else {
 #pragma unroll
                         for (int j = 0; j < BN / 64; ++j)
@@ -575,23 +615,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const int kb1 = args.k_splits > 1 ? min(k_blocks, kb0 + args.k_per_split) : k_blocks;
             float4 pre[8];
             if constexpr (MODE == MODE_GRADW) {
-                // first chunk of the accumulator's old values, read before the tile's MMAs finish
-                const int64_t row = static_cast<int64_t>(m) * BM + q * 32 + lane;
+                // first block of the accumulator's old values, read before the tile's MMAs finish
                 const int64_t c0 = static_cast<int64_t>(n) * BN + 128 * half;
-                if (!args.acc_first && row < m_rows && c0 < args.N) {
-                    const float* p0 = args.out_f32 + row * args.ld_f32 + c0;
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) pre[g] = *reinterpret_cast<const float4*>(p0 + 4 * g);
-                } else {
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) pre[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+                if (!args.acc_first && c0 < args.N)
+                    gradw_load_old(args, static_cast<int64_t>(m) * BM + q * 32, m_rows, c0, lane, pre);
             }
             if (!wait_phase(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, args.status, limit)) break;
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             epilogue_tile<MODE>(args, m, n, q, half, lane, taddr, smem_u32(&ctl->tmem_empty[acc]), m_rows,
-                                kb1 <= kb0, ks, pre);
+                                kb1 <= kb0, ks, pre, epi_stage);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -605,8 +638,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 }
 
 template <int MODE>
-cudaError_t launch_gemm_mode(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
-                             int grid, cudaStream_t stream) {
+cudaError_t launch_gemm_single(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
+                               int grid, cudaStream_t stream) {
     static std::atomic<uint64_t> configured{0};  // bit d: shared-memory limit raised on device d
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -614,11 +647,11 @@ cudaError_t launch_gemm_mode(const CUtensorMap& map_a, const CUtensorMap& map_b,
     const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
     if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GEMM_SMEM_BYTES);
+                                 gemm_smem_bytes(MODE, false));
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_release);
     }
-    gemm_kernel<MODE><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(map_a, map_b, args);
+    gemm_kernel<MODE><<<grid, GEMM_THREADS, gemm_smem_bytes(MODE, false), stream>>>(map_a, map_b, args);
     return cudaGetLastError();
 }
 

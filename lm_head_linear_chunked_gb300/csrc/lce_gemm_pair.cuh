@@ -1,0 +1,314 @@
+// The pair form of the library's GEMM: a cluster of two CTAs on neighbouring
+// SMs shares each 256 x 256 output tile through one tcgen05.mma of M = 256
+// (cta_group::2), issued by rank 0.  Each CTA loads its own 128 rows of A
+// and its own half of B (128 of the tile's 256 columns), so a 64-element K
+// slice costs each SM 32 KB of shared memory and L2 traffic instead of the
+// single-CTA form's 48 KB, and the ring is 6 stages deep instead of 4.
+//
+//   warp 0 (one lane, both CTAs): TMA producer of the CTA's own halves.
+//          Both CTAs' copies of a slice complete on rank 0's `full` barrier
+//          (the pair form of the TMA load), which rank 0 arms for both.
+//   warp 1 (one lane, rank 0): MMA issuer.  Commits go to both CTAs'
+//          barriers (multicast): `empty` frees the slot in both rings,
+//          `tmem_full` starts both epilogues.
+//   warps 2..9 (both CTAs): the epilogue of the CTA's 128 rows, the same
+//          code as the single-CTA form; each warp hands the accumulator back
+//          by arriving on rank 0's `tmem_empty`.
+//
+// Every wait is bounded.  A wait that runs out raises the status bit and
+// both CTAs' abort flags; before exiting, each CTA waits (bounded) until the
+// MMAs' completion signals for its ring have arrived and the peer has
+// finished, so that no signal or read reaches a CTA that has exited.
+#pragma once
+
+#include "lce_gemm.cuh"
+
+namespace lce {
+
+struct SharedCtlPair {
+    uint64_t full[PAIR_STAGES];
+    uint64_t empty[PAIR_STAGES];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t drain;
+    uint64_t fin;
+    uint32_t tmem_base;
+    volatile int abort_flag;
+};
+static_assert(sizeof(SharedCtlPair) <= CTL_BYTES, "pair control block too large");
+
+// wait_phase of the pair form: running out also raises the peer's abort
+// flag.  The acquire stays at CTA scope: these barriers order TMA copies,
+// MMAs and TMEM reads, and no wait here orders data the peer's threads wrote.
+__device__ __forceinline__ bool wait_phase_pair(uint32_t bar, uint32_t parity, SharedCtlPair* ctl,
+                                                uint32_t peer_abort, unsigned* status, uint64_t limit_ns,
+                                                bool honor_abort = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (honor_abort && ctl->abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            ctl->abort_flag = 1;
+            st_shared_cluster_u32(peer_abort, 1u);
+            atomicOr(status, STATUS_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                     const GemmArgs args) {
+    using T = ModeTraits<MODE>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle needs 1024-byte alignment
+    SharedCtlPair* ctl =
+        reinterpret_cast<SharedCtlPair*>(smem_raw + (base - raw) + PAIR_STAGES * PAIR_STAGE_BYTES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint64_t limit = args.timeout_ns;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+    // grad_W epilogue: this warp's block buffer (launched with the extra bytes)
+    float* const epi_stage =
+        reinterpret_cast<float*>(smem_raw + (base - raw) + PAIR_STAGES * PAIR_STAGE_BYTES + CTL_BYTES) +
+        (warp >= 2 ? (warp - 2) * EPI_STAGE_FLOATS : 0);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PAIR_STAGES; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&ctl->tmem_full[b]), 1);
+            mbar_init(smem_u32(&ctl->tmem_empty[b]), 2 * EPI_WARPS);
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        mbar_init(smem_u32(&ctl->fin), 1);
+        ctl->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&map_a);
+        tma_prefetch_map(&map_b);
+    }
+    // Both CTAs' barriers exist before either CTA signals the other.
+    __syncwarp();
+    cluster_sync_all();
+    if (warp == 1) tmem_alloc_pair(smem_u32(&ctl->tmem_base), TMEM_COLS);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const uint32_t peer_abort = map_shared_rank(smem_u32(const_cast<int*>(&ctl->abort_flag)), peer);
+
+    const int num_tiles = args.m_tiles * args.n_tiles * (args.k_splits > 1 ? args.k_splits : 1);
+    const int cid = static_cast<int>(blockIdx.x >> 1);
+    const int ncl = static_cast<int>(gridDim.x >> 1);
+    const int dyn = args.dyn_rows ? *args.dyn_rows : -1;
+    const int64_t m_rows = (MODE == MODE_GRADX && dyn >= 0) ? static_cast<int64_t>(dyn) : args.M;
+    const int k_blocks = (MODE == MODE_GRADW && dyn >= 0) ? (dyn + BK - 1) / BK : args.k_blocks;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (this CTA's halves)
+            uint32_t stage = 0, phase = 0;
+            uint64_t issued = 0;
+            bool ok = true;
+            for (int t = cid; t < num_tiles && ok; t += ncl) {
+                int m, n, ks;
+                tile_and_slice(t, args, m, n, ks);
+                if (static_cast<int64_t>(m) * PAIR_BM >= m_rows) continue;
+                const int kb0 = args.k_splits > 1 ? ks * args.k_per_split : 0;
+                const int kb1 = args.k_splits > 1 ? min(k_blocks, kb0 + args.k_per_split) : k_blocks;
+                const int32_t arow = m * PAIR_BM + static_cast<int32_t>(rank) * BM;
+                const int32_t bcol = n * BN + static_cast<int32_t>(rank) * (BN / 2);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_phase_pair(smem_u32(&ctl->empty[stage]), phase ^ 1u, ctl, peer_abort, args.status,
+                                         limit)) {
+                        ok = false;
+                        break;
+                    }
+                    // rank 0's barrier counts both CTAs' bytes of the slice
+                    const uint32_t fb = map_shared_rank(smem_u32(&ctl->full[stage]), 0);
+                    if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[stage]), 2 * PAIR_STAGE_BYTES);
+                    const uint32_t sa = base + stage * PAIR_STAGE_BYTES;
+                    const uint32_t sb = sa + A_STAGE_BYTES;
+                    const int32_t k0 = kb * BK;
+                    if constexpr (!T::A_MN) {
+                        tma_load_2d_pair(sa, &map_a, fb, k0, args.a_y0 + arow);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BM / 64; ++j)
+                            tma_load_2d_pair(sa + j * 8192, &map_a, fb, arow + 64 * j, args.a_y0 + k0);
+                    }
+                    if constexpr (!T::B_MN) {
+                        tma_load_2d_pair(sb, &map_b, fb, k0, args.b_y0 + bcol);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < (BN / 2) / 64; ++j)
+                            tma_load_2d_pair(sb + j * 8192, &map_b, fb, bcol + 64 * j, args.b_y0 + k0);
+                    }
+                    ++issued;
+                    if (++stage == PAIR_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            const uint64_t last = issued < PAIR_STAGES ? issued : PAIR_STAGES;
+            if (!ok) {
+                // Let this CTA's copies still in flight land before it exits:
+                // rank 0 watches them on its barriers (which count both
+                // CTAs' bytes); rank 1, whose copies complete there too,
+                // gives them a fixed 100 us, far longer than a copy takes.
+                if (rank == 0) {
+                    for (uint64_t i = 0; i < last; ++i) {
+                        const uint64_t j = issued - 1 - i;
+                        wait_phase_pair(smem_u32(&ctl->full[j % PAIR_STAGES]),
+                                        static_cast<uint32_t>((j / PAIR_STAGES) & 1u), ctl, peer_abort, args.status,
+                                        limit, false);
+                    }
+                } else {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (globaltimer_ns() - t0 < 100000ull) {
+                    }
+                }
+            } else {
+                // Wait for the MMA completions that free the last slots: they
+                // arrive on this CTA's barriers, also from rank 0.
+                for (uint64_t i = 0; i < last; ++i) {
+                    const uint64_t j = issued - 1 - i;
+                    if (!wait_phase_pair(smem_u32(&ctl->empty[j % PAIR_STAGES]),
+                                         static_cast<uint32_t>((j / PAIR_STAGES) & 1u), ctl, peer_abort,
+                                         args.status, limit, false))
+                        break;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // ---------------- MMA issuer (rank 0)
+            constexpr uint32_t IDESC = instr_desc_f16kind(PAIR_BM, BN, T::A_MN, T::B_MN, T::F16);
+            constexpr uint32_t A_STEP = T::A_MN ? (2048u >> 4) : (32u >> 4);
+            constexpr uint32_t B_STEP = T::B_MN ? (2048u >> 4) : (32u >> 4);
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = cid; t < num_tiles && ok; t += ncl) {
+                int m, n, ks;
+                tile_and_slice(t, args, m, n, ks);
+                if (static_cast<int64_t>(m) * PAIR_BM >= m_rows) continue;
+                const int kb0 = args.k_splits > 1 ? ks * args.k_per_split : 0;
+                const int kb1 = args.k_splits > 1 ? min(k_blocks, kb0 + args.k_per_split) : k_blocks;
+                if (!wait_phase_pair(smem_u32(&ctl->tmem_empty[acc]), acc_phase ^ 1u, ctl, peer_abort, args.status,
+                                     limit)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_phase_pair(smem_u32(&ctl->full[stage]), phase, ctl, peer_abort, args.status, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = base + stage * PAIR_STAGE_BYTES;
+                    const uint32_t sb = sa + A_STAGE_BYTES;
+                    const uint64_t adesc = T::A_MN ? smem_desc_sw128(sa, 8192, 1024) : smem_desc_sw128(sa, 16, 1024);
+                    const uint64_t bdesc = T::B_MN ? smem_desc_sw128(sb, 8192, 1024) : smem_desc_sw128(sb, 16, 1024);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        mma_f16kind_pair(d_tmem, adesc + A_STEP * k, bdesc + B_STEP * k, IDESC,
+                                         (kb != kb0 || k != 0) ? 1u : 0u);
+                    mma_commit_pair_multicast(smem_u32(&ctl->empty[stage]), 0x3);
+                    if (++stage == PAIR_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit_pair_multicast(smem_u32(&ctl->tmem_full[acc]), 0x3);
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok) {
+                // Wait for every MMA this thread issued before TMEM is freed.
+                mma_commit_pair(smem_u32(&ctl->drain));
+                wait_phase_pair(smem_u32(&ctl->drain), 0, ctl, peer_abort, args.status, limit, false);
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2..9) of this CTA's 128 rows
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        uint32_t acc = 0, acc_phase = 0;
+        for (int t = cid; t < num_tiles; t += ncl) {
+            int m, n, ks;
+            tile_and_slice(t, args, m, n, ks);
+            if (static_cast<int64_t>(m) * PAIR_BM >= m_rows) continue;
+            const int kb0 = args.k_splits > 1 ? ks * args.k_per_split : 0;
+            const int kb1 = args.k_splits > 1 ? min(k_blocks, kb0 + args.k_per_split) : k_blocks;
+            const int mc = 2 * m + static_cast<int>(rank);  // this CTA's 128-row tile
+            float4 pre[8];
+            if constexpr (MODE == MODE_GRADW) {
+                const int64_t c0 = static_cast<int64_t>(n) * BN + 128 * half;
+                if (!args.acc_first && c0 < args.N)
+                    gradw_load_old(args, static_cast<int64_t>(mc) * BM + q * 32, m_rows, c0, lane, pre);
+            }
+            if (!wait_phase_pair(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, peer_abort, args.status, limit))
+                break;
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+            epilogue_tile<MODE, true>(args, mc, n, q, half, lane, taddr,
+                                      map_shared_rank(smem_u32(&ctl->tmem_empty[acc]), 0), m_rows, kb1 <= kb0, ks,
+                                      pre, epi_stage);
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    __syncwarp();  // reconverge the producer and MMA warps (one lane worked)
+    tc_fence_before_sync();
+    __syncthreads();
+    // Neither CTA leaves (or frees TMEM) before the other is done with it.
+    if (threadIdx.x == 0) {
+        mbar_arrive_cluster(map_shared_rank(smem_u32(&ctl->fin), peer));
+        wait_phase_pair(smem_u32(&ctl->fin), 0, ctl, peer_abort, args.status, limit, false);
+    }
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
+template <int MODE>
+cudaError_t launch_gemm_pair(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args, int grid,
+                             cudaStream_t stream) {
+    static std::atomic<uint64_t> configured{0};  // bit d: shared-memory limit raised on device d
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (grid <= 0 || (grid & 1)) return cudaErrorInvalidConfiguration;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+    if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 gemm_smem_bytes(MODE, true));
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_release);
+    }
+    gemm_pair_kernel<MODE><<<grid, GEMM_THREADS, gemm_smem_bytes(MODE, true), stream>>>(map_a, map_b, args);
+    return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_gemm_mode(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args, int grid,
+                             cudaStream_t stream, bool pair) {
+    return pair ? launch_gemm_pair<MODE>(map_a, map_b, args, grid, stream)
+                : launch_gemm_single<MODE>(map_a, map_b, args, grid, stream);
+}
+
+}  // namespace lce

@@ -34,9 +34,33 @@ constexpr int B_STAGE_BYTES = BN * BK * 2;                 // 32 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES; // 48 KB
 constexpr int CTL_BYTES = 256;
 constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + CTL_BYTES;
+// K-major B operands are loaded as boxes of 128 rows (two per 256-row tile
+// here; one per CTA in the pair form below).
+constexpr int B_BOX_ROWS = 128;
 constexpr int EPI_WARPS = 8;        // two per TMEM lane quarter, one per 128-column half
 constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
 constexpr uint32_t TMEM_COLS = 512; // two 256-column fp32 accumulators
+
+// Pair form: two CTAs on neighbouring SMs (a cluster of 2) share one
+// tcgen05 MMA of M = 256, N = 256 (cta_group::2).  Each CTA loads its own
+// 128 rows of A and its own 128 rows (or columns) of B per 64-element K
+// slice, 32 KB a stage instead of 48 KB, so the ring is 6 deep; each CTA's
+// TMEM holds its 128 rows of the two accumulators.
+constexpr int PAIR_BM = 2 * BM;                                      // 256 rows per pair tile
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_B_STAGE_BYTES = (BN / 2) * BK * 2;                // 16 KB
+constexpr int PAIR_STAGE_BYTES = A_STAGE_BYTES + PAIR_B_STAGE_BYTES; // 32 KB
+constexpr int GEMM_PAIR_SMEM_BYTES = 1024 + PAIR_STAGES * PAIR_STAGE_BYTES + CTL_BYTES;
+
+// The grad_W epilogue passes each warp's 32x32 FP32 blocks through a 4 KB
+// shared-memory buffer per epilogue warp (after the ring and control block).
+constexpr int EPI_STAGE_FLOATS = 32 * 32;
+constexpr int EPI_STAGE_BYTES = EPI_WARPS * EPI_STAGE_FLOATS * 4;  // 32 KB
+constexpr int gemm_smem_bytes(int mode, bool pair) {
+    return (pair ? GEMM_PAIR_SMEM_BYTES : GEMM_SMEM_BYTES) + (mode == MODE_GRADW ? EPI_STAGE_BYTES : 0);
+}
+static_assert(GEMM_SMEM_BYTES + EPI_STAGE_BYTES <= 232448 && GEMM_PAIR_SMEM_BYTES + EPI_STAGE_BYTES <= 232448,
+              "shared memory of one CTA");
 
 // Device status word bits (bit k set = lce_status_t k was raised).
 constexpr unsigned STATUS_LABEL = 1u << LCE_ERR_LABEL_RANGE;
@@ -136,16 +160,21 @@ struct GemmArgs {
     uint64_t timeout_ns;
 };
 
-// Launches the GEMM kernel of `mode`.  The instantiations are spread over
-// three translation units so that they compile in parallel.
+// Launches the GEMM kernel of `mode`: with `pair`, the pair form (grid =
+// 2 x the number of pairs; m_tiles counts 256-row tiles), else one CTA per
+// 128-row tile (grid = CTAs).  The instantiations are spread over three
+// translation units so that they compile in parallel.
 cudaError_t launch_gemm(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                        const GemmArgs& args, int grid, cudaStream_t stream);
+                        const GemmArgs& args, int grid, cudaStream_t stream, bool pair);
 cudaError_t launch_gemm_logits(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                               const GemmArgs& args, int grid, cudaStream_t stream);
+                               const GemmArgs& args, int grid, cudaStream_t stream, bool pair);
 cudaError_t launch_gemm_grads(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                              const GemmArgs& args, int grid, cudaStream_t stream);
+                              const GemmArgs& args, int grid, cudaStream_t stream, bool pair);
 cudaError_t launch_gemm_plain(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                              const GemmArgs& args, int grid, cudaStream_t stream);
+                              const GemmArgs& args, int grid, cudaStream_t stream, bool pair);
+// Pairs of the pair form that can be resident at once on this device (0 if
+// the form cannot launch).
+int gemm_pair_slots();
 
 // Small kernels (lce_aux.cu).
 cudaError_t launch_prepass(const int64_t* y, int64_t N, int64_t V, int64_t ignore_index,

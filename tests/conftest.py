@@ -13,6 +13,15 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: large workload, minutes of CPU oracle time")
 
 
+def pytest_sessionstart(session):
+    # LCE_TEST_GEMM_FORM=single|pair runs the whole suite with that GEMM form
+    # instead of the library's default.
+    form = os.environ.get("LCE_TEST_GEMM_FORM")
+    if form:
+        import lm_head_linear_chunked_gb300 as lce
+        lce.lce_set_gemm_form(form)
+
+
 def pytest_collection_modifyitems(config, items):
     # GPU tests are skipped, not failed, where no GPU is present; the CPU
     # suite deselects them with -m "not gpu" anyway.
