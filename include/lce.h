@@ -216,6 +216,7 @@ LCE_API lce_status_t lce_forward_static_ws(int64_t N, int64_t H, int64_t V,
 
 /* lce_set_gemm_form: the tensor-core GEMM form of the calls this process
  * makes after it (each call reads the setting once, when it is made).
+ * The default is LCE_GEMM_PAIR.
  *   LCE_GEMM_SINGLE: one CTA per SM computes 128x256 output tiles with
  *     tcgen05.mma cta_group::1 and a 4-stage ring of 48 KB slices.
  *   LCE_GEMM_PAIR: a cluster of two CTAs on neighbouring SMs computes

@@ -145,6 +145,22 @@ bool map_16bit_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, 
     return r == CUDA_SUCCESS;
 }
 
+// Row-major FP32 matrix [rows, cols] with row pitch `pitch` elements, boxes
+// of 32 x 32 (128-byte rows, 128-byte swizzle): the grad_W accumulator as
+// the target of the epilogue's tile stores and adds.
+bool map_f32_acc(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t pitch) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch) * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
     static std::atomic<int> cached[64];
     int dev = 0;
@@ -159,7 +175,7 @@ int sm_count() {
 }
 
 // The GEMM form of this process's calls (lce_set_gemm_form), read once per call.
-std::atomic<int> g_gemm_form{LCE_GEMM_SINGLE};
+std::atomic<int> g_gemm_form{LCE_GEMM_PAIR};
 
 struct Form {
     bool pair;
@@ -313,6 +329,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     if (!map_16bit_2d(&mX_k, pb.X, pb.N, pb.H, pb.H, 64, BM) || !map_16bit_2d(&mW_k, pb.W, pb.V, pb.H, pb.H, 64, B_BOX_ROWS))
         return LCE_ERR_CUDA;
     if (do_bwd && !map_16bit_2d(&mW16_mn, W16, pb.V, pb.H, pb.H, 64, 64, true)) return LCE_ERR_CUDA;
+    CUtensorMap mAcc{};
+    if (do_bwd && !map_f32_acc(&mAcc, o.grad_W_acc, pb.V, pb.H, pb.H)) return LCE_ERR_CUDA;
 
     LCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
     if (counts) LCE_TRY_CUDA(cudaMemsetAsync(counts, 0, static_cast<size_t>(pb.V) * 4, s));
@@ -359,7 +377,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.ldg = p.ldg;
                 a.row_map = dmap + r0;
             }
-            LCE_LAUNCH(PK_LSE, launch_gemm(MODE_LSE, mX_k, mW_k, a, grid_of(form, mtf * p.n_vt), s, form.pair));
+            LCE_LAUNCH(PK_LSE, launch_gemm(MODE_LSE, mX_k, mW_k, mW_k, a, grid_of(form, mtf * p.n_vt), s, form.pair));
             LCE_LAUNCH(PK_OTHER, launch_combine(pm, ps, 2 * p.n_vt, p.C, rows, zt, pb.y + r0, pb.ignore_index, o.lse + r0,
                                         row_loss + r0, s));
         }
@@ -386,7 +404,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.ldg = p.ldg;
                 a.gb_part = gb;
                 a.row_map = dmap + r0;
-                LCE_LAUNCH(PK_P, launch_gemm(MODE_G, mX_k, mW_k, a, grid_of(form, mtf * p.n_vt), s, form.pair));
+                LCE_LAUNCH(PK_P, launch_gemm(MODE_G, mX_k, mW_k, mW_k, a, grid_of(form, mtf * p.n_vt), s, form.pair));
             }
             if (gb)
                 LCE_LAUNCH(PK_OTHER, launch_grad_b(gb, mt * 4, pb.V, hdr, counts, o.grad_b_acc, o.grad_b, first, last, s));
@@ -422,7 +440,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.k_per_split = static_cast<int32_t>(cdiv(a.k_blocks, p.gradx_splits));
                 a.split_out = split_out;
                 a.split_stride = p.C * pb.H;
-                LCE_LAUNCH(PK_GRADX, launch_gemm(MODE_GRADX, mG_k, mW16_mn, a,
+                LCE_LAUNCH(PK_GRADX, launch_gemm(MODE_GRADX, mG_k, mW16_mn, mW16_mn, a,
                                                  grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles *
                                                                    p.gradx_splits),
                                                  s, form.pair));
@@ -447,9 +465,10 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                 a.ld_out = pb.H;
                 a.acc_first = first;
                 a.write_bf16 = last && o.grad_W != nullptr;
+                a.acc_tma = 1;
                 a.b_amax_bits = &hdr->amax_x_bits;
                 a.dyn_rows = nvc + c;
-                LCE_LAUNCH(PK_GRADW, launch_gemm(MODE_GRADW, mG_mn, mX16_mn, a,
+                LCE_LAUNCH(PK_GRADW, launch_gemm(MODE_GRADW, mG_mn, mX16_mn, mAcc, a,
                                                  grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles), s,
                                                  form.pair));
             }
@@ -469,15 +488,15 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
 
 }  // namespace
 
-cudaError_t launch_gemm(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
-                        int grid, cudaStream_t stream, bool pair) {
+cudaError_t launch_gemm(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_c,
+                        const GemmArgs& args, int grid, cudaStream_t stream, bool pair) {
     if (grid <= 0) return cudaErrorInvalidConfiguration;
     switch (mode) {
         case MODE_LSE:
-        case MODE_G: return launch_gemm_logits(mode, map_a, map_b, args, grid, stream, pair);
+        case MODE_G: return launch_gemm_logits(mode, map_a, map_b, map_c, args, grid, stream, pair);
         case MODE_GRADX:
-        case MODE_GRADW: return launch_gemm_grads(mode, map_a, map_b, args, grid, stream, pair);
-        default: return launch_gemm_plain(mode, map_a, map_b, args, grid, stream, pair);
+        case MODE_GRADW: return launch_gemm_grads(mode, map_a, map_b, map_c, args, grid, stream, pair);
+        default: return launch_gemm_plain(mode, map_a, map_b, map_c, args, grid, stream, pair);
     }
 }
 
@@ -651,7 +670,7 @@ lce_status_t lce_debug_gemm(int layout, int64_t M, int64_t N, int64_t K, const l
     a.out_f32 = D;
     a.ld_f32 = N;
     LCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
-    LCE_TRY_CUDA(launch_gemm(layout, ma, mb, a, grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles), s,
+    LCE_TRY_CUDA(launch_gemm(layout, ma, mb, mb, a, grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles), s,
                              form.pair));
     return LCE_OK;
 }

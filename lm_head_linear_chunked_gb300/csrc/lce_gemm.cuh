@@ -189,6 +189,13 @@ __device__ __forceinline__ float warp_column_sums(float (&g)[32], int lane) {
     return g[0];
 }
 
+// Whether the grad_W epilogue reads the accumulator's old values into the
+// SM (the read-modify-write path): not on the first chunk, and not when the
+// tile is added into the accumulator at L2 by a TMA reduce.
+__device__ __forceinline__ bool gradw_reads_old(const GemmArgs& a) {
+    return !a.acc_first && (a.write_bf16 || !a.acc_tma);
+}
+
 // The FP32 grad_W accumulator values a warp's lane reads for the 32x32 block
 // at rows row_base .. +31, columns c0 .. c0+31: rows (lane >> 3) + 4i
 // (i = 0..7), columns c0 + 4 (lane & 7) .. +3; rows past m_rows read as 0.
@@ -219,7 +226,8 @@ __device__ __forceinline__ void release_acc(uint32_t bar) {
 template <int MODE, bool PAIR = false>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, int q, int half, int lane,
                                               uint32_t taddr, uint32_t empty_bar, int64_t m_rows,
-                                              bool zero_acc, int ks, const float4 (&pre)[8], float* stage) {
+                                              bool zero_acc, int ks, const float4 (&pre)[8], float* stage,
+                                              const CUtensorMap* map_c) {
     const int64_t row = static_cast<int64_t>(m) * BM + q * 32 + lane;
     const int64_t col0 = static_cast<int64_t>(n) * BN;
     const int j0 = half * (BN / 64);  // this warp's four 32-column chunks: half of the tile's columns
@@ -371,6 +379,40 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         // (the first block by the caller, before the tile's MMAs finished).
         const float s = ldexpf(*a.scale, -(P_SCALE_EXP + operand_scale_exp(*a.b_amax_bits)));
         const int64_t row_base = static_cast<int64_t>(m) * BM + q * 32;
+        if (a.acc_tma && !a.write_bf16) {
+            // s * block -> buffer -> one TMA store (first chunk) or add at L2
+            // (later chunks) per 32x32 block; the accumulator never passes
+            // through the SM.  The buffer is the TMA box's 128-byte-swizzled
+            // layout: row r's 16-byte slot k at slot k ^ (r & 7).
+            const uint32_t sbuf = smem_u32(stage);
+#pragma unroll 1
+            for (int jj = 0; jj < BN / 64; ++jj) {
+                const int64_t c0 = col0 + 32 * (j0 + jj);
+                if (c0 >= a.N) break;
+                float v[32];
+                tmem_load_32cols(taddr + 32 * (j0 + jj), v);
+                if (lane == 0) bulk_wait_read_all();  // the previous block has left the buffer
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<float4*>(stage + lane * 32 + ((k ^ (lane & 7)) << 2)) =
+                        zero_acc ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                 : make_float4(s * v[4 * k], s * v[4 * k + 1], s * v[4 * k + 2], s * v[4 * k + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && row_base < m_rows) {
+                    if (a.acc_first)
+                        tma_store_2d(map_c, sbuf, static_cast<int32_t>(c0), static_cast<int32_t>(row_base));
+                    else
+                        tma_reduce_add_2d(map_c, sbuf, static_cast<int32_t>(c0), static_cast<int32_t>(row_base));
+                    bulk_commit_group();
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) release_acc<PAIR>(empty_bar);
+            return;
+        }
         const int g = lane & 7;
         float4 cur[8];
 #pragma unroll
@@ -445,18 +487,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
 template <int MODE>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                const GemmArgs args) {
+                const __grid_constant__ CUtensorMap map_c, const GemmArgs args) {
     using T = ModeTraits<MODE>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle needs 1024-byte alignment
-    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem_raw + (base - raw) + STAGES * STAGE_BYTES);
+    // ring | grad_W block buffers (MODE_GRADW) | control block
+    constexpr int EPI_BYTES = MODE == MODE_GRADW ? EPI_STAGE_BYTES : 0;
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem_raw + (base - raw) + STAGES * STAGE_BYTES + EPI_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint64_t limit = args.timeout_ns;
     // grad_W epilogue: this warp's block buffer (launched with the extra bytes)
-    float* const epi_stage = reinterpret_cast<float*>(smem_raw + (base - raw) + STAGES * STAGE_BYTES + CTL_BYTES) +
+    float* const epi_stage = reinterpret_cast<float*>(smem_raw + (base - raw) + STAGES * STAGE_BYTES) +
                              (warp >= 2 ? (warp - 2) * EPI_STAGE_FLOATS : 0);
 
     if (threadIdx.x == 0) {
@@ -475,6 +519,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&map_a);
         tma_prefetch_map(&map_b);
+        if (MODE == MODE_GRADW && args.acc_tma) tma_prefetch_map(&map_c);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
@@ -617,20 +662,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if constexpr (MODE == MODE_GRADW) {
                 // first block of the accumulator's old values, read before the tile's MMAs finish
                 const int64_t c0 = static_cast<int64_t>(n) * BN + 128 * half;
-                if (!args.acc_first && c0 < args.N)
+                if (gradw_reads_old(args) && c0 < args.N)
                     gradw_load_old(args, static_cast<int64_t>(m) * BM + q * 32, m_rows, c0, lane, pre);
             }
             if (!wait_phase(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, args.status, limit)) break;
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             epilogue_tile<MODE>(args, m, n, q, half, lane, taddr, smem_u32(&ctl->tmem_empty[acc]), m_rows,
-                                kb1 <= kb0, ks, pre, epi_stage);
+                                kb1 <= kb0, ks, pre, epi_stage, &map_c);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
     }
 
     __syncwarp();  // reconverge the producer and MMA warps (one lane worked)
+    // the epilogue's tile stores/adds read this CTA's shared memory until done
+    if (MODE == MODE_GRADW && warp >= 2 && lane == 0) bulk_wait_all();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -638,8 +685,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 }
 
 template <int MODE>
-cudaError_t launch_gemm_single(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
-                               int grid, cudaStream_t stream) {
+cudaError_t launch_gemm_single(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_c,
+                               const GemmArgs& args, int grid, cudaStream_t stream) {
     static std::atomic<uint64_t> configured{0};  // bit d: shared-memory limit raised on device d
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -651,7 +698,7 @@ cudaError_t launch_gemm_single(const CUtensorMap& map_a, const CUtensorMap& map_
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_release);
     }
-    gemm_kernel<MODE><<<grid, GEMM_THREADS, gemm_smem_bytes(MODE, false), stream>>>(map_a, map_b, args);
+    gemm_kernel<MODE><<<grid, GEMM_THREADS, gemm_smem_bytes(MODE, false), stream>>>(map_a, map_b, map_c, args);
     return cudaGetLastError();
 }
 

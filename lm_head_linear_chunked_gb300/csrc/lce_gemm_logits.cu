@@ -4,11 +4,11 @@
 
 namespace lce {
 
-cudaError_t launch_gemm_logits(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_gemm_logits(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_c,
                                const GemmArgs& args, int grid, cudaStream_t stream, bool pair) {
     switch (mode) {
-        case MODE_LSE: return launch_gemm_mode<MODE_LSE>(map_a, map_b, args, grid, stream, pair);
-        case MODE_G: return launch_gemm_mode<MODE_G>(map_a, map_b, args, grid, stream, pair);
+        case MODE_LSE: return launch_gemm_mode<MODE_LSE>(map_a, map_b, map_c, args, grid, stream, pair);
+        case MODE_G: return launch_gemm_mode<MODE_G>(map_a, map_b, map_c, args, grid, stream, pair);
         default: return cudaErrorInvalidValue;
     }
 }

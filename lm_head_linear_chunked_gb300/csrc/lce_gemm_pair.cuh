@@ -60,13 +60,15 @@ __device__ __forceinline__ bool wait_phase_pair(uint32_t bar, uint32_t parity, S
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                     const GemmArgs args) {
+                     const __grid_constant__ CUtensorMap map_c, const GemmArgs args) {
     using T = ModeTraits<MODE>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle needs 1024-byte alignment
+    // ring | grad_W block buffers (MODE_GRADW) | control block
+    constexpr int EPI_BYTES = MODE == MODE_GRADW ? EPI_STAGE_BYTES : 0;
     SharedCtlPair* ctl =
-        reinterpret_cast<SharedCtlPair*>(smem_raw + (base - raw) + PAIR_STAGES * PAIR_STAGE_BYTES);
+        reinterpret_cast<SharedCtlPair*>(smem_raw + (base - raw) + PAIR_STAGES * PAIR_STAGE_BYTES + EPI_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -74,9 +76,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
     // grad_W epilogue: this warp's block buffer (launched with the extra bytes)
-    float* const epi_stage =
-        reinterpret_cast<float*>(smem_raw + (base - raw) + PAIR_STAGES * PAIR_STAGE_BYTES + CTL_BYTES) +
-        (warp >= 2 ? (warp - 2) * EPI_STAGE_FLOATS : 0);
+    float* const epi_stage = reinterpret_cast<float*>(smem_raw + (base - raw) + PAIR_STAGES * PAIR_STAGE_BYTES) +
+                             (warp >= 2 ? (warp - 2) * EPI_STAGE_FLOATS : 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < PAIR_STAGES; ++s) {
@@ -95,6 +96,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&map_a);
         tma_prefetch_map(&map_b);
+        if (MODE == MODE_GRADW && args.acc_tma) tma_prefetch_map(&map_c);
     }
     // Both CTAs' barriers exist before either CTA signals the other.
     __syncwarp();
@@ -257,7 +259,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             float4 pre[8];
             if constexpr (MODE == MODE_GRADW) {
                 const int64_t c0 = static_cast<int64_t>(n) * BN + 128 * half;
-                if (!args.acc_first && c0 < args.N)
+                if (gradw_reads_old(args) && c0 < args.N)
                     gradw_load_old(args, static_cast<int64_t>(mc) * BM + q * 32, m_rows, c0, lane, pre);
             }
             if (!wait_phase_pair(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, peer_abort, args.status, limit))
@@ -266,13 +268,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             epilogue_tile<MODE, true>(args, mc, n, q, half, lane, taddr,
                                       map_shared_rank(smem_u32(&ctl->tmem_empty[acc]), 0), m_rows, kb1 <= kb0, ks,
-                                      pre, epi_stage);
+                                      pre, epi_stage, &map_c);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
     }
 
     __syncwarp();  // reconverge the producer and MMA warps (one lane worked)
+    // the epilogue's tile stores/adds read this CTA's shared memory until done
+    if (MODE == MODE_GRADW && warp >= 2 && lane == 0) bulk_wait_all();
     tc_fence_before_sync();
     __syncthreads();
     // Neither CTA leaves (or frees TMEM) before the other is done with it.
@@ -286,8 +290,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 }
 
 template <int MODE>
-cudaError_t launch_gemm_pair(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args, int grid,
-                             cudaStream_t stream) {
+cudaError_t launch_gemm_pair(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_c,
+                             const GemmArgs& args, int grid, cudaStream_t stream) {
     static std::atomic<uint64_t> configured{0};  // bit d: shared-memory limit raised on device d
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -300,15 +304,15 @@ cudaError_t launch_gemm_pair(const CUtensorMap& map_a, const CUtensorMap& map_b,
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_release);
     }
-    gemm_pair_kernel<MODE><<<grid, GEMM_THREADS, gemm_smem_bytes(MODE, true), stream>>>(map_a, map_b, args);
+    gemm_pair_kernel<MODE><<<grid, GEMM_THREADS, gemm_smem_bytes(MODE, true), stream>>>(map_a, map_b, map_c, args);
     return cudaGetLastError();
 }
 
 template <int MODE>
-cudaError_t launch_gemm_mode(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args, int grid,
-                             cudaStream_t stream, bool pair) {
-    return pair ? launch_gemm_pair<MODE>(map_a, map_b, args, grid, stream)
-                : launch_gemm_single<MODE>(map_a, map_b, args, grid, stream);
+cudaError_t launch_gemm_mode(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_c,
+                             const GemmArgs& args, int grid, cudaStream_t stream, bool pair) {
+    return pair ? launch_gemm_pair<MODE>(map_a, map_b, map_c, args, grid, stream)
+                : launch_gemm_single<MODE>(map_a, map_b, map_c, args, grid, stream);
 }
 
 }  // namespace lce

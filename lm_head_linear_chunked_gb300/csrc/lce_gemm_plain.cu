@@ -4,12 +4,12 @@
 
 namespace lce {
 
-cudaError_t launch_gemm_plain(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_gemm_plain(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_c,
                               const GemmArgs& args, int grid, cudaStream_t stream, bool pair) {
     switch (mode) {
-        case MODE_PLAIN_KK: return launch_gemm_mode<MODE_PLAIN_KK>(map_a, map_b, args, grid, stream, pair);
-        case MODE_PLAIN_KM: return launch_gemm_mode<MODE_PLAIN_KM>(map_a, map_b, args, grid, stream, pair);
-        case MODE_PLAIN_MM: return launch_gemm_mode<MODE_PLAIN_MM>(map_a, map_b, args, grid, stream, pair);
+        case MODE_PLAIN_KK: return launch_gemm_mode<MODE_PLAIN_KK>(map_a, map_b, map_c, args, grid, stream, pair);
+        case MODE_PLAIN_KM: return launch_gemm_mode<MODE_PLAIN_KM>(map_a, map_b, map_c, args, grid, stream, pair);
+        case MODE_PLAIN_MM: return launch_gemm_mode<MODE_PLAIN_MM>(map_a, map_b, map_c, args, grid, stream, pair);
         default: return cudaErrorInvalidValue;
     }
 }

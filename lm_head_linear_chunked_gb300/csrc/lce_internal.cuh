@@ -53,7 +53,8 @@ constexpr int PAIR_STAGE_BYTES = A_STAGE_BYTES + PAIR_B_STAGE_BYTES; // 32 KB
 constexpr int GEMM_PAIR_SMEM_BYTES = 1024 + PAIR_STAGES * PAIR_STAGE_BYTES + CTL_BYTES;
 
 // The grad_W epilogue passes each warp's 32x32 FP32 blocks through a 4 KB
-// shared-memory buffer per epilogue warp (after the ring and control block).
+// shared-memory buffer per epilogue warp (after the ring, before the control
+// block; 1024-byte aligned, laid out as a 128-byte-swizzled TMA box).
 constexpr int EPI_STAGE_FLOATS = 32 * 32;
 constexpr int EPI_STAGE_BYTES = EPI_WARPS * EPI_STAGE_FLOATS * 4;  // 32 KB
 constexpr int gemm_smem_bytes(int mode, bool pair) {
@@ -138,6 +139,8 @@ struct GemmArgs {
     int64_t ld_f32;
     int32_t acc_first;   // MODE_GRADW: overwrite instead of accumulate
     int32_t write_bf16;  // MODE_GRADW: also write the bf16 cast
+    int32_t acc_tma;     // MODE_GRADW: without write_bf16, store (first) or add (later) the tile into
+                         // out_f32 through the third tensor map (FP32 [M, N], 32x32 boxes, 128-byte swizzle)
     // Valid-row compaction: the backward products skip ignored rows.
     //   MODE_LSE / MODE_G: row_map[chunk row] = row of the compacted P it is
     //     stored at (-1: ignored, not stored).
@@ -164,13 +167,14 @@ struct GemmArgs {
 // 2 x the number of pairs; m_tiles counts 256-row tiles), else one CTA per
 // 128-row tile (grid = CTAs).  The instantiations are spread over three
 // translation units so that they compile in parallel.
-cudaError_t launch_gemm(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
+// map_c: the grad_W accumulator's map (MODE_GRADW with acc_tma), else unused.
+cudaError_t launch_gemm(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_c,
                         const GemmArgs& args, int grid, cudaStream_t stream, bool pair);
-cudaError_t launch_gemm_logits(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_gemm_logits(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_c,
                                const GemmArgs& args, int grid, cudaStream_t stream, bool pair);
-cudaError_t launch_gemm_grads(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_gemm_grads(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_c,
                               const GemmArgs& args, int grid, cudaStream_t stream, bool pair);
-cudaError_t launch_gemm_plain(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
+cudaError_t launch_gemm_plain(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_c,
                               const GemmArgs& args, int grid, cudaStream_t stream, bool pair);
 // Pairs of the pair form that can be resident at once on this device (0 if
 // the form cannot launch).
