@@ -12,8 +12,10 @@ exactly to double):
   lse[i]    = m_i + ln sum_v exp(z[i, v] - m_i),      m_i = max_v z[i, v]
   valid(i)  = y[i] != ignore_index
   n_valid   = #{i : valid(i)}
-  loss      = (1 / n_valid) sum_{valid i} (lse[i] - z[i, y[i]])
-  s         = grad_scale * grad_output / n_valid
+  loss      = (1 / n_valid) sum_{valid i} (lse[i] - z[i, y[i]])   (reduction "mean")
+            =               sum_{valid i} (lse[i] - z[i, y[i]])   (reduction "sum")
+  s         = grad_scale * grad_output / n_valid                  (mean)
+            = grad_scale * grad_output                            (sum)
   G[i, v]   = s (exp(z[i, v] - lse[i]) - [v == y[i]])  for valid i, else 0
   grad_X    = G W,   grad_W = G^T X,   grad_b = sum_i G[i, :]
 
@@ -25,6 +27,9 @@ Sources, by page and section:
   grad_bias are accumulated in FP32 and cast back to the weight dtype.
 * Same page, section 3 (`BaseTrainer.fit`): the loss is normalised by the
   count of valid (non-ignored) tokens, with a guard against dividing by zero.
+  That count is gathered over all ranks and micro-batches before the
+  division, so a trainer may instead take the plain sum of a micro-batch's
+  per-token losses and divide by its own count: reduction "sum".
 * TRL "1M 토큰 이상 학습" page, section "매우 큰 logits 행렬: 청킹": the loss
   is a sum over rows and the softmax runs along one row's vocabulary, so
   any split of the rows gives the same result.  That is why this oracle may
@@ -93,8 +98,13 @@ def check_labels(y: np.ndarray, V: int, ignore_index: int = IGNORE_INDEX) -> Non
         raise ValueError(f"label out of range at row {int(np.argmax(bad))}")
 
 
-def grad_scale_per_row(grad_scale: float, grad_output: float, n_valid: int) -> float:
-    """s = grad_scale * grad_output / n_valid; 0 when there is no valid row."""
+def grad_scale_per_row(grad_scale: float, grad_output: float, n_valid: int, reduction: str = "mean") -> float:
+    """s = grad_scale * grad_output / n_valid (mean; 0 when there is no valid
+    row), or grad_scale * grad_output (sum)."""
+    if reduction == "sum":
+        return float(grad_scale) * float(grad_output)
+    if reduction != "mean":
+        raise ValueError(f"reduction must be 'mean' or 'sum', got {reduction!r}")
     if n_valid == 0:
         return 0.0
     return float(grad_scale) * float(grad_output) / n_valid
@@ -120,7 +130,7 @@ def _pool(threads: Optional[int]):
 
 
 def forward(X, W, b, y, ignore_index: int = IGNORE_INDEX, block_rows: int = 256,
-            threads: Optional[int] = None) -> dict:
+            threads: Optional[int] = None, reduction: str = "mean") -> dict:
     """loss, lse [N] and n_valid of the whole problem."""
     X, W, b = as_f64(X), as_f64(W), as_f64(b)
     y = np.asarray(y, dtype=np.int64)
@@ -141,13 +151,19 @@ def forward(X, W, b, y, ignore_index: int = IGNORE_INDEX, block_rows: int = 256,
         list(ex.map(one, _blocks(N, block_rows)))
     ok = valid_mask(y, ignore_index)
     n_valid = int(ok.sum())
-    loss = float((lse[ok] - zt[ok]).sum() / n_valid) if n_valid else 0.0
+    total = float((lse[ok] - zt[ok]).sum())
+    if reduction == "sum":
+        loss = total
+    elif reduction == "mean":
+        loss = total / n_valid if n_valid else 0.0
+    else:
+        raise ValueError(f"reduction must be 'mean' or 'sum', got {reduction!r}")
     return {"loss": loss, "lse": lse, "n_valid": n_valid}
 
 
 def backward(X, W, b, y, lse, ignore_index: int = IGNORE_INDEX, grad_scale: float = 1.0,
              grad_output: float = 1.0, block_rows: int = 256,
-             threads: Optional[int] = None) -> dict:
+             threads: Optional[int] = None, reduction: str = "mean") -> dict:
     """grad_X [N,H], grad_W [V,H], grad_b [V] (None without a bias), given lse."""
     X, W, b = as_f64(X), as_f64(W), as_f64(b)
     y = np.asarray(y, dtype=np.int64)
@@ -155,7 +171,7 @@ def backward(X, W, b, y, lse, ignore_index: int = IGNORE_INDEX, grad_scale: floa
     N, H = X.shape
     V = W.shape[0]
     check_labels(y, V, ignore_index)
-    s = grad_scale_per_row(grad_scale, grad_output, count_valid(y, ignore_index))
+    s = grad_scale_per_row(grad_scale, grad_output, count_valid(y, ignore_index), reduction)
     grad_X = np.zeros((N, H))
     blocks = _blocks(N, block_rows)
     part_W = [None] * len(blocks)
@@ -180,10 +196,11 @@ def backward(X, W, b, y, lse, ignore_index: int = IGNORE_INDEX, grad_scale: floa
 
 
 def fused(X, W, b, y, ignore_index: int = IGNORE_INDEX, grad_scale: float = 1.0,
-          grad_output: float = 1.0, block_rows: int = 256, threads: Optional[int] = None) -> dict:
+          grad_output: float = 1.0, block_rows: int = 256, threads: Optional[int] = None,
+          reduction: str = "mean") -> dict:
     """forward() then backward() with the forward's lse."""
-    f = forward(X, W, b, y, ignore_index, block_rows, threads)
-    g = backward(X, W, b, y, f["lse"], ignore_index, grad_scale, grad_output, block_rows, threads)
+    f = forward(X, W, b, y, ignore_index, block_rows, threads, reduction)
+    g = backward(X, W, b, y, f["lse"], ignore_index, grad_scale, grad_output, block_rows, threads, reduction)
     f.update(g)
     return f
 

@@ -211,6 +211,59 @@ def pin_torch_cross_entropy(orc):
     return fails
 
 
+def pin_torch_cross_entropy_sum(orc):
+    """Reduction "sum" against torch CPU float64 F.cross_entropy(...,
+    reduction="sum") with autograd: loss, and every gradient scaled by
+    grad_scale * grad_output (no division by n_valid)."""
+    import torch
+    fails = []
+    for seed, bias, gs, go in ((16, True, 1.0, 1.0), (17, False, 0.25, 2.0)):
+        X, W, b, y = tiny_problem(seed, N=9, H=10, V=19, bias=bias, ignore=(2, 5))
+        out = orc.fused(X, W, b, y, grad_scale=gs, grad_output=go, reduction="sum")
+        tX = torch.tensor(X, requires_grad=True)
+        tW = torch.tensor(W, requires_grad=True)
+        tb = torch.tensor(b, requires_grad=True) if b is not None else None
+        z = tX @ tW.T + (tb if tb is not None else 0.0)
+        loss = torch.nn.functional.cross_entropy(z, torch.tensor(y), ignore_index=IGN, reduction="sum")
+        (loss * gs).backward(torch.tensor(go, dtype=torch.float64))
+        if abs(out["loss"] - loss.item()) > 1e-12 * max(1.0, abs(loss.item())):
+            fails.append(f"P8s loss {out['loss']} vs torch {loss.item()} (seed {seed})")
+        for k, t in (("grad_X", tX), ("grad_W", tW)):
+            if not _close(out[k], t.grad.numpy(), 1e-11):
+                fails.append(f"P8s {k} (seed {seed})")
+        if tb is not None and not _close(out["grad_b"], tb.grad.numpy(), 1e-11):
+            fails.append(f"P8s grad_b (seed {seed})")
+    # no valid row: the empty sum is 0 and so is every gradient
+    X, W, b, y = tiny_problem(18, N=3, H=4, V=5, ignore=(0, 1, 2))
+    out = orc.fused(X, W, b, y, reduction="sum")
+    if out["loss"] != 0.0 or np.abs(out["grad_W"]).max() != 0.0:
+        fails.append("P8s all rows ignored")
+    return fails
+
+
+def pin_finite_differences_sum(orc):
+    """Central differences of the summed loss match the reduction "sum" gradients."""
+    X, W, b, y = tiny_problem(19, N=5, H=6, V=7, ignore=(3,))
+    out = orc.fused(X, W, b, y, reduction="sum")
+    eps = 1e-6
+    fails = []
+    for name, arr, grad in (("W", W, out["grad_W"]), ("b", b, out["grad_b"])):
+        num = np.zeros_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            p = arr.copy(); p[idx] += eps
+            m = arr.copy(); m[idx] -= eps
+            args_p = {"W": (X, p, b), "b": (X, W, p)}[name]
+            args_m = {"W": (X, m, b), "b": (X, W, m)}[name]
+            num[idx] = (orc.forward(*args_p, y, reduction="sum")["loss"] -
+                        orc.forward(*args_m, y, reduction="sum")["loss"]) / (2 * eps)
+        err = np.abs(num - grad).max() / max(np.abs(grad).max(), 1e-30)
+        if not err <= 1e-6:
+            fails.append(f"P5s finite differences for {name}: rel err {err:.2e}")
+    return fails
+
+
 def pin_single_class(orc):
     """V = 1: the only class has probability 1, so loss = 0 and all grads = 0."""
     X, W, b, y = tiny_problem(10, N=5, H=4, V=1, ignore=(1,))
@@ -316,7 +369,8 @@ def pin_row_sampled_pieces(orc):
 
 ALL_PINS = [pin_zero_weight_closed_form, pin_rows_sum_to_zero, pin_ignored_rows,
             pin_finite_differences, pin_shift_invariance, pin_row_permutation,
-            pin_torch_cross_entropy, pin_single_class, pin_no_valid_rows,
+            pin_torch_cross_entropy, pin_torch_cross_entropy_sum, pin_finite_differences_sum,
+            pin_single_class, pin_no_valid_rows,
             pin_worked_example, pin_block_invariance, pin_row_sampled_pieces]
 
 

@@ -29,8 +29,11 @@ MUTANTS = {
     "grad_X_shifted_weight": ("        grad_X[r0:r1] = G @ W\n",
                                  "        grad_X[r0:r1] = G @ np.roll(W, 1, axis=1)\n"),
     "grad_b_wrong_axis": ("        part_b[j] = G.sum(axis=0)\n", "        part_b[j] = G.sum(axis=1).sum() + 0 * G.sum(axis=0)\n"),
-    "mean_over_all_rows": ("    loss = float((lse[ok] - zt[ok]).sum() / n_valid) if n_valid else 0.0\n",
-                           "    loss = float((lse[ok] - zt[ok]).sum() / N) if n_valid else 0.0\n"),
+    "mean_over_all_rows": ("        loss = total / n_valid if n_valid else 0.0\n",
+                           "        loss = total / N if n_valid else 0.0\n"),
+    "sum_loss_divided": ("        loss = total\n", "        loss = total / max(n_valid, 1)\n"),
+    "sum_scale_divided": ("        return float(grad_scale) * float(grad_output)\n",
+                          "        return float(grad_scale) * float(grad_output) / max(n_valid, 1)\n"),
     "target_logit_wrong_column": ("        zt[r0:r1][ok] = z[np.nonzero(ok)[0], yy[ok]]\n",
                                   "        zt[r0:r1][ok] = z[np.nonzero(ok)[0], 0]\n"),
 }
