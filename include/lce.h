@@ -140,6 +140,44 @@ LCE_API lce_status_t lce_fused_fwd_bwd(int64_t N, int64_t H, int64_t V,
                                float* grad_W_acc, float* grad_b_acc,
                                void* ws, size_t ws_bytes, lce_stream_t stream);
 
+/* The same three calls with option flags (flags = 0 is the call above):
+ *   LCE_REDUCTION_SUM: loss is the sum, not the mean, of the valid rows'
+ *     cross-entropies, and the gradient scale is grad_scale * grad_output
+ *     without the division by n_valid.  A trainer that normalises by a
+ *     token count of its own (LlamaFactory PR #10762 analysis page, section
+ *     3: the valid-token count gathered over all ranks and micro-batches)
+ *     passes its 1/count as grad_scale.
+ *   LCE_ACCUMULATE (backward and fused only): grad_W_acc and grad_b_acc
+ *     hold a running FP32 total (gradient accumulation over micro-batches)
+ *     and this call adds its gradients to them instead of overwriting
+ *     them; grad_W and grad_b receive the cast of the new totals.  grad_X
+ *     is written, as always.  The caller zeroes the accumulators before
+ *     the first call of a total.
+ * Unknown bits, or LCE_ACCUMULATE given to lce_forward_ex, return
+ * LCE_ERR_INVALID_ARG before anything is enqueued. */
+#define LCE_REDUCTION_SUM 1u
+#define LCE_ACCUMULATE 2u
+LCE_API lce_status_t lce_forward_ex(int64_t N, int64_t H, int64_t V,
+                            const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
+                            const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
+                            float* loss, float* lse, int64_t* n_valid,
+                            void* ws, size_t ws_bytes, lce_stream_t stream, uint32_t flags);
+LCE_API lce_status_t lce_backward_ex(int64_t N, int64_t H, int64_t V,
+                             const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
+                             const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
+                             const float* lse, float grad_scale, const float* d_grad_output,
+                             lce_bf16* grad_X, lce_bf16* grad_W, lce_bf16* grad_b,
+                             float* grad_W_acc, float* grad_b_acc,
+                             void* ws, size_t ws_bytes, lce_stream_t stream, uint32_t flags);
+LCE_API lce_status_t lce_fused_fwd_bwd_ex(int64_t N, int64_t H, int64_t V,
+                                  const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
+                                  const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
+                                  float grad_scale, const float* d_grad_output,
+                                  float* loss, float* lse, int64_t* n_valid,
+                                  lce_bf16* grad_X, lce_bf16* grad_W, lce_bf16* grad_b,
+                                  float* grad_W_acc, float* grad_b_acc,
+                                  void* ws, size_t ws_bytes, lce_stream_t stream, uint32_t flags);
+
 /* The backward of the chunk-loss plugin's saved-gradient design (LlamaFactory
  * PR #10762 analysis page, section 4: the Function computes the gradients in
  * its forward, and its backward scales them by grad_output).  After an

@@ -52,6 +52,12 @@ _SIGS = {
                      _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "lce_fused_fwd_bwd": [_I64, _I64, _I64, _P, _P, _P, _P, _I64, _I64, ctypes.c_float, _P,
                           _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "lce_forward_ex": [_I64, _I64, _I64, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _P, ctypes.c_size_t, _P,
+                       ctypes.c_uint32],
+    "lce_backward_ex": [_I64, _I64, _I64, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_float, _P,
+                        _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_uint32],
+    "lce_fused_fwd_bwd_ex": [_I64, _I64, _I64, _P, _P, _P, _P, _I64, _I64, ctypes.c_float, _P,
+                             _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_uint32],
     "lce_check_status": [_P, _P],
     "lce_status_string": [_STATUS],
     "lce_debug_gemm": [ctypes.c_int, _I64, _I64, _I64, _P, _P, _P, _P, ctypes.c_size_t, _P],
@@ -155,6 +161,43 @@ def lce_fused_fwd_bwd(N, H, V, X, W, b, y, ignore_index, chunk_rows, grad_scale,
            "lce_fused_fwd_bwd")
 
 
+REDUCTION_SUM = 1   # LCE_REDUCTION_SUM
+ACCUMULATE = 2      # LCE_ACCUMULATE
+
+
+def lce_forward_ex(N, H, V, X, W, b, y, ignore_index, chunk_rows, loss, lse, n_valid, ws, ws_bytes, stream,
+                   flags) -> None:
+    _check(lib().lce_forward_ex(N, H, V, _ptr(X), _ptr(W), _ptr(b), _ptr(y), ignore_index, chunk_rows,
+                                _ptr(loss), _ptr(lse), _ptr(n_valid), _ptr(ws), ws_bytes, _stream(stream),
+                                int(flags)),
+           "lce_forward_ex")
+
+
+def lce_backward_ex(N, H, V, X, W, b, y, ignore_index, chunk_rows, lse, grad_scale, d_grad_output,
+                    grad_X, grad_W, grad_b, grad_W_acc, grad_b_acc, ws, ws_bytes, stream, flags) -> None:
+    _check(lib().lce_backward_ex(N, H, V, _ptr(X), _ptr(W), _ptr(b), _ptr(y), ignore_index, chunk_rows,
+                                 _ptr(lse), float(grad_scale), _ptr(d_grad_output), _ptr(grad_X), _ptr(grad_W),
+                                 _ptr(grad_b), _ptr(grad_W_acc), _ptr(grad_b_acc), _ptr(ws), ws_bytes,
+                                 _stream(stream), int(flags)),
+           "lce_backward_ex")
+
+
+def lce_fused_fwd_bwd_ex(N, H, V, X, W, b, y, ignore_index, chunk_rows, grad_scale, d_grad_output, loss, lse,
+                         n_valid, grad_X, grad_W, grad_b, grad_W_acc, grad_b_acc, ws, ws_bytes, stream,
+                         flags) -> None:
+    _check(lib().lce_fused_fwd_bwd_ex(N, H, V, _ptr(X), _ptr(W), _ptr(b), _ptr(y), ignore_index, chunk_rows,
+                                      float(grad_scale), _ptr(d_grad_output), _ptr(loss), _ptr(lse),
+                                      _ptr(n_valid), _ptr(grad_X), _ptr(grad_W), _ptr(grad_b), _ptr(grad_W_acc),
+                                      _ptr(grad_b_acc), _ptr(ws), ws_bytes, _stream(stream), int(flags)),
+           "lce_fused_fwd_bwd_ex")
+
+
+def _flags(reduction: str, accumulate: bool) -> int:
+    if reduction not in ("mean", "sum"):
+        raise ValueError(f"reduction must be 'mean' or 'sum', got {reduction!r}")
+    return (REDUCTION_SUM if reduction == "sum" else 0) | (ACCUMULATE if accumulate else 0)
+
+
 STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -241,8 +284,8 @@ def workspace(N, H, V, chunk_rows=0, has_bias=False, which=WS_FUSED, device="cud
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def forward(X, W, b, y, ignore_index=IGNORE_INDEX, chunk_rows=0, ws=None, stream=None):
-    """loss, lse, n_valid of the chunked linear cross-entropy (one lce_forward call)."""
+def forward(X, W, b, y, ignore_index=IGNORE_INDEX, chunk_rows=0, ws=None, stream=None, reduction="mean"):
+    """loss, lse, n_valid of the chunked linear cross-entropy (one lce_forward_ex call)."""
     torch = _torch()
     N, H = X.shape
     V = W.shape[0]
@@ -253,56 +296,78 @@ def forward(X, W, b, y, ignore_index=IGNORE_INDEX, chunk_rows=0, ws=None, stream
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     n_valid = torch.empty(1, dtype=torch.int64, device=dev)
     stream = stream or torch.cuda.current_stream(dev)
-    lce_forward(N, H, V, _bits(X), _bits(W), _bits(b), y, ignore_index, chunk_rows, loss, lse, n_valid,
-                ws, ws.numel(), stream)
+    lce_forward_ex(N, H, V, _bits(X), _bits(W), _bits(b), y, ignore_index, chunk_rows, loss, lse, n_valid,
+                   ws, ws.numel(), stream, _flags(reduction, False))
     return {"loss": loss, "lse": lse, "n_valid": n_valid, "ws": ws}
 
 
+def _accumulators(W, b, accumulate, grad_W_acc, grad_b_acc):
+    """The FP32 accumulators: the caller's (required with accumulate), else new ones."""
+    torch = _torch()
+    V = W.shape[0]
+    if accumulate:
+        if grad_W_acc is None or (b is not None and grad_b_acc is None):
+            raise ValueError("accumulate=True needs the running grad_W_acc (and grad_b_acc with a bias)")
+        return grad_W_acc, grad_b_acc
+    gw = grad_W_acc if grad_W_acc is not None else torch.empty(W.shape, dtype=torch.float32, device=W.device)
+    gb = None
+    if b is not None:
+        gb = grad_b_acc if grad_b_acc is not None else torch.empty(V, dtype=torch.float32, device=W.device)
+    return gw, gb
+
+
 def backward(X, W, b, y, lse, ignore_index=IGNORE_INDEX, chunk_rows=0, grad_scale=1.0, grad_output=None,
-             want_grad_X=True, ws=None, stream=None):
+             want_grad_X=True, ws=None, stream=None, reduction="mean", accumulate=False, grad_W_acc=None,
+             grad_b_acc=None):
+    """All gradients from a forward's lse (one lce_backward_ex call).  With
+    accumulate=True the given FP32 accumulators are added to."""
     torch = _torch()
     N, H = X.shape
     V = W.shape[0]
     dev = X.device
     if ws is None:
         ws = workspace(N, H, V, chunk_rows, b is not None, WS_BACKWARD, dev)
+    gw_acc, gb_acc = _accumulators(W, b, accumulate, grad_W_acc, grad_b_acc)
     out = {
         "grad_X": torch.empty_like(X) if want_grad_X else None,
         "grad_W": torch.empty_like(W),
-        "grad_W_acc": torch.empty(W.shape, dtype=torch.float32, device=dev),
+        "grad_W_acc": gw_acc,
         "grad_b": torch.empty_like(b) if b is not None else None,
-        "grad_b_acc": torch.empty(V, dtype=torch.float32, device=dev) if b is not None else None,
+        "grad_b_acc": gb_acc,
         "ws": ws,
     }
     stream = stream or torch.cuda.current_stream(dev)
-    lce_backward(N, H, V, _bits(X), _bits(W), _bits(b), y, ignore_index, chunk_rows, lse, grad_scale, grad_output,
-                 out["grad_X"], out["grad_W"], out["grad_b"], out["grad_W_acc"], out["grad_b_acc"], ws, ws.numel(),
-                 stream)
+    lce_backward_ex(N, H, V, _bits(X), _bits(W), _bits(b), y, ignore_index, chunk_rows, lse, grad_scale,
+                    grad_output, out["grad_X"], out["grad_W"], out["grad_b"], out["grad_W_acc"], out["grad_b_acc"],
+                    ws, ws.numel(), stream, _flags(reduction, accumulate))
     return out
 
 
 def fused(X, W, b, y, ignore_index=IGNORE_INDEX, chunk_rows=0, grad_scale=1.0, grad_output=None, ws=None,
-          stream=None):
-    """loss, lse, n_valid and all gradients (one lce_fused_fwd_bwd call)."""
+          stream=None, reduction="mean", accumulate=False, grad_W_acc=None, grad_b_acc=None):
+    """loss, lse, n_valid and all gradients (one lce_fused_fwd_bwd_ex call).
+    With accumulate=True the given FP32 accumulators are added to."""
     torch = _torch()
     N, H = X.shape
     V = W.shape[0]
     dev = X.device
     if ws is None:
         ws = workspace(N, H, V, chunk_rows, b is not None, WS_FUSED, dev)
+    gw_acc, gb_acc = _accumulators(W, b, accumulate, grad_W_acc, grad_b_acc)
     out = {
         "loss": torch.empty(1, dtype=torch.float32, device=dev),
         "lse": torch.empty(N, dtype=torch.float32, device=dev),
         "n_valid": torch.empty(1, dtype=torch.int64, device=dev),
         "grad_X": torch.empty_like(X),
         "grad_W": torch.empty_like(W),
-        "grad_W_acc": torch.empty(W.shape, dtype=torch.float32, device=dev),
+        "grad_W_acc": gw_acc,
         "grad_b": torch.empty_like(b) if b is not None else None,
-        "grad_b_acc": torch.empty(V, dtype=torch.float32, device=dev) if b is not None else None,
+        "grad_b_acc": gb_acc,
         "ws": ws,
     }
     stream = stream or torch.cuda.current_stream(dev)
-    lce_fused_fwd_bwd(N, H, V, _bits(X), _bits(W), _bits(b), y, ignore_index, chunk_rows, grad_scale, grad_output,
-                      out["loss"], out["lse"], out["n_valid"], out["grad_X"], out["grad_W"], out["grad_b"],
-                      out["grad_W_acc"], out["grad_b_acc"], ws, ws.numel(), stream)
+    lce_fused_fwd_bwd_ex(N, H, V, _bits(X), _bits(W), _bits(b), y, ignore_index, chunk_rows, grad_scale,
+                         grad_output, out["loss"], out["lse"], out["n_valid"], out["grad_X"], out["grad_W"],
+                         out["grad_b"], out["grad_W_acc"], out["grad_b_acc"], ws, ws.numel(), stream,
+                         _flags(reduction, accumulate))
     return out

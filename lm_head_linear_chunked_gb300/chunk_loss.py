@@ -8,10 +8,10 @@ and cast), and whose backward only scales those saved gradients by the
 incoming grad_output; and a module that replaces an nn.Linear head's
 forward with the loss.
 
-Here the forward is one lce_fused_fwd_bwd call and the backward one
+Here the forward is one lce_fused_fwd_bwd_ex call and the backward one
 lce_scale_grads call; all arithmetic runs in the library's kernels (torch
 only allocates the outputs).  With torch.is_grad_enabled() false, or when
-nothing needs a gradient, the forward is a plain lce_forward.
+nothing needs a gradient, the forward is a plain lce_forward_ex.
 """
 from __future__ import annotations
 
@@ -19,7 +19,7 @@ from typing import Optional
 
 import torch
 
-from . import IGNORE_INDEX, WS_FORWARD, WS_FUSED, lce_check_status, lce_forward, lce_fused_fwd_bwd, \
+from . import IGNORE_INDEX, WS_FORWARD, WS_FUSED, _flags, lce_check_status, lce_forward_ex, lce_fused_fwd_bwd_ex, \
     lce_scale_grads, lce_workspace_size
 
 
@@ -29,11 +29,11 @@ def _flat_contiguous(t: torch.Tensor) -> torch.Tensor:
 
 
 class ChunkedLinearCrossEntropy(torch.autograd.Function):
-    """loss = mean over valid rows of cross_entropy(hidden @ weight.T + bias, labels)."""
+    """loss = mean (or sum) over valid rows of cross_entropy(hidden @ weight.T + bias, labels)."""
 
     @staticmethod
     def forward(ctx, hidden, weight, bias, labels, ignore_index: int, chunk_rows: int, check: bool,
-                grad_wanted: bool):
+                grad_wanted: bool, reduction: str = "mean"):
         X = _flat_contiguous(hidden)
         y = labels.reshape(-1).to(torch.int64).contiguous()
         N, H = X.shape
@@ -42,21 +42,23 @@ class ChunkedLinearCrossEntropy(torch.autograd.Function):
         stream = torch.cuda.current_stream(dev)
         # (forward runs with autograd off; the caller says whether a graph is built)
         want_grads = grad_wanted and any(ctx.needs_input_grad[:3])
+        flags = _flags(reduction, False)
         loss = torch.empty(1, dtype=torch.float32, device=dev)
         lse = torch.empty(N, dtype=torch.float32, device=dev)
         n_valid = torch.empty(1, dtype=torch.int64, device=dev)
         if not want_grads:
             nws = lce_workspace_size(N, H, V, chunk_rows, bias is not None, WS_FORWARD)
             ws = torch.empty(nws, dtype=torch.uint8, device=dev)
-            lce_forward(N, H, V, X, weight, bias, y, ignore_index, chunk_rows, loss, lse, n_valid, ws, nws, stream)
+            lce_forward_ex(N, H, V, X, weight, bias, y, ignore_index, chunk_rows, loss, lse, n_valid, ws, nws, stream,
+                           flags)
         else:
             nws = lce_workspace_size(N, H, V, chunk_rows, bias is not None, WS_FUSED)
             ws = torch.empty(nws, dtype=torch.uint8, device=dev)
             grad_X = torch.empty_like(X)
             grad_W_acc = torch.empty((V, H), dtype=torch.float32, device=dev)
             grad_b_acc = torch.empty(V, dtype=torch.float32, device=dev) if bias is not None else None
-            lce_fused_fwd_bwd(N, H, V, X, weight, bias, y, ignore_index, chunk_rows, 1.0, None, loss, lse, n_valid,
-                              grad_X, None, None, grad_W_acc, grad_b_acc, ws, nws, stream)
+            lce_fused_fwd_bwd_ex(N, H, V, X, weight, bias, y, ignore_index, chunk_rows, 1.0, None, loss, lse,
+                                 n_valid, grad_X, None, None, grad_W_acc, grad_b_acc, ws, nws, stream, flags)
             ctx.save_for_backward(grad_X, grad_W_acc, grad_b_acc)
             ctx.shape = (tuple(hidden.shape), N, H, V)
             ctx.dtypes = (weight.dtype, bias.dtype if bias is not None else None)
@@ -81,25 +83,28 @@ class ChunkedLinearCrossEntropy(torch.autograd.Function):
                         grad_b_acc if grad_b is not None else None, grad_b,
                         torch.cuda.current_stream(grad_X.device))
         gx = grad_X.reshape(shape) if ctx.needs_input_grad[0] else None
-        return gx, grad_W, grad_b, None, None, None, None, None
+        return gx, grad_W, grad_b, None, None, None, None, None, None
 
 
 def linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor, labels: torch.Tensor,
                          bias: Optional[torch.Tensor] = None, ignore_index: int = IGNORE_INDEX,
-                         chunk_rows: int = 0, check: bool = False, return_lse: bool = False):
+                         chunk_rows: int = 0, check: bool = False, return_lse: bool = False,
+                         reduction: str = "mean"):
     """Chunked linear cross-entropy with autograd.
 
     hidden [..., H] bf16, weight [V, H] bf16 (nn.Linear layout), labels [...]
     with ignore_index for ignored positions, bias [V] or None.  Returns the
-    mean loss over valid positions (0 if none), and the per-row logsumexp if
-    return_lse.  chunk_rows = 0 lets the library choose.  check=True
-    synchronises and raises on a device-side error (bad label)."""
+    mean (reduction="mean") or sum (reduction="sum") of the loss over valid
+    positions (0 if none), and the per-row logsumexp if return_lse.
+    chunk_rows = 0 lets the library choose.  check=True synchronises and
+    raises on a device-side error (bad label)."""
     if chunk_rows < 0:
         raise ValueError("chunk_rows must not be negative")
+    _flags(reduction, False)  # validates reduction
     grad_wanted = torch.is_grad_enabled() and any(
         t is not None and t.requires_grad for t in (hidden, weight, bias))
     loss, lse = ChunkedLinearCrossEntropy.apply(hidden, weight, bias, labels, ignore_index, chunk_rows, check,
-                                                grad_wanted)
+                                                grad_wanted, reduction)
     return (loss, lse) if return_lse else loss
 
 
@@ -107,14 +112,17 @@ class ChunkLoss(torch.nn.Module):
     """Wraps an nn.Linear LM head so that head(hidden, labels) returns the loss
     (the plugin's replacement of the head's forward), never the logits."""
 
-    def __init__(self, head: torch.nn.Linear, chunk_rows: int = 0, ignore_index: int = IGNORE_INDEX):
+    def __init__(self, head: torch.nn.Linear, chunk_rows: int = 0, ignore_index: int = IGNORE_INDEX,
+                 reduction: str = "mean"):
         super().__init__()
         if chunk_rows < 0:
             raise ValueError("chunk_rows must not be negative")
+        _flags(reduction, False)
         self.head = head
         self.chunk_rows = chunk_rows
         self.ignore_index = ignore_index
+        self.reduction = reduction
 
     def forward(self, hidden: torch.Tensor, labels: torch.Tensor) -> torch.Tensor:
         return linear_cross_entropy(hidden, self.head.weight, labels, self.head.bias, self.ignore_index,
-                                    self.chunk_rows)
+                                    self.chunk_rows, reduction=self.reduction)

@@ -278,6 +278,7 @@ struct Outputs {
     const float* d_grad_output;
     uint16_t *grad_X, *grad_W, *grad_b;
     float *grad_W_acc, *grad_b_acc;
+    uint32_t flags;  // LCE_REDUCTION_SUM | LCE_ACCUMULATE
 };
 
 lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, int64_t chunk_rows, void* ws,
@@ -301,6 +302,10 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             return LCE_ERR_INVALID_ARG;
         }
     }
+    if (o.flags & ~(LCE_REDUCTION_SUM | LCE_ACCUMULATE)) return LCE_ERR_INVALID_ARG;
+    if ((o.flags & LCE_ACCUMULATE) && !do_bwd) return LCE_ERR_INVALID_ARG;
+    const bool sum_reduction = (o.flags & LCE_REDUCTION_SUM) != 0;
+    const bool accumulate = (o.flags & LCE_ACCUMULATE) != 0;
     if (ws_bytes < p.total) return LCE_ERR_WORKSPACE;
     if (!encode_fn() || sm_count() <= 0) return LCE_ERR_CUDA;
     const Form form = gemm_form();
@@ -336,7 +341,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     if (counts) LCE_TRY_CUDA(cudaMemsetAsync(counts, 0, static_cast<size_t>(pb.V) * 4, s));
     LCE_LAUNCH(PK_OTHER, launch_prepass(pb.y, pb.N, pb.V, pb.ignore_index, hdr, counts, s));
     if (do_bwd) {
-        LCE_LAUNCH(PK_OTHER, launch_scale(hdr, o.grad_scale, o.d_grad_output, nullptr, s));
+        LCE_LAUNCH(PK_OTHER, launch_scale(hdr, o.grad_scale, o.d_grad_output, nullptr, sum_reduction, s));
         LCE_LAUNCH(PK_OTHER, launch_label_sort(pb.y, pb.N, p.C, p.label_blocks_per_chunk,
                                        p.n_chunks * p.label_blocks_per_chunk, pb.V, pb.ignore_index, keys, runs,
                                        nrun, s));
@@ -382,7 +387,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                                         row_loss + r0, s));
         }
         if (do_bwd) {
-            const bool first = c == 0, last = c == p.n_chunks - 1;
+            // first: the chunk that overwrites the FP32 accumulators (none when accumulating)
+            const bool first = c == 0 && !accumulate, last = c == p.n_chunks - 1;
             if (do_fwd) {  // P = E 2^(tile max - lse), in place
                 LCE_LAUNCH(PK_OTHER, launch_p_rescale(G, p.ldg, rows, pb.V, pm, p.C, o.lse + r0, crow + r0, nvc + c,
                                                       gb, s));
@@ -482,7 +488,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             }
         }
     }
-    if (do_fwd) LCE_LAUNCH(PK_OTHER, launch_loss(row_loss, pb.N, hdr, o.loss, o.n_valid, s));
+    if (do_fwd) LCE_LAUNCH(PK_OTHER, launch_loss(row_loss, pb.N, hdr, o.loss, o.n_valid, sum_reduction, s));
     return LCE_OK;
 }
 
@@ -522,23 +528,31 @@ lce_status_t lce_chunk_rows(int64_t N, int64_t H, int64_t V, int64_t chunk_rows,
     return st;
 }
 
-lce_status_t lce_forward(int64_t N, int64_t H, int64_t V, const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
-                         const int64_t* y, int64_t ignore_index, int64_t chunk_rows, float* loss, float* lse,
-                         int64_t* n_valid, void* ws, size_t ws_bytes, lce_stream_t stream) {
+lce_status_t lce_forward_ex(int64_t N, int64_t H, int64_t V, const lce_bf16* X, const lce_bf16* W,
+                            const lce_bf16* b, const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
+                            float* loss, float* lse, int64_t* n_valid, void* ws, size_t ws_bytes,
+                            lce_stream_t stream, uint32_t flags) {
     Problem pb{N, H, V, X, W, b, y, ignore_index};
     Outputs o;
     memset(&o, 0, sizeof(o));
     o.loss = loss;
     o.lse = lse;
     o.n_valid = n_valid;
+    o.flags = flags;
     return run(pb, o, true, false, chunk_rows, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
-lce_status_t lce_backward(int64_t N, int64_t H, int64_t V, const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
-                          const int64_t* y, int64_t ignore_index, int64_t chunk_rows, const float* lse,
-                          float grad_scale, const float* d_grad_output, lce_bf16* grad_X, lce_bf16* grad_W,
-                          lce_bf16* grad_b, float* grad_W_acc, float* grad_b_acc, void* ws, size_t ws_bytes,
-                          lce_stream_t stream) {
+lce_status_t lce_forward(int64_t N, int64_t H, int64_t V, const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
+                         const int64_t* y, int64_t ignore_index, int64_t chunk_rows, float* loss, float* lse,
+                         int64_t* n_valid, void* ws, size_t ws_bytes, lce_stream_t stream) {
+    return lce_forward_ex(N, H, V, X, W, b, y, ignore_index, chunk_rows, loss, lse, n_valid, ws, ws_bytes, stream, 0);
+}
+
+lce_status_t lce_backward_ex(int64_t N, int64_t H, int64_t V, const lce_bf16* X, const lce_bf16* W,
+                             const lce_bf16* b, const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
+                             const float* lse, float grad_scale, const float* d_grad_output, lce_bf16* grad_X,
+                             lce_bf16* grad_W, lce_bf16* grad_b, float* grad_W_acc, float* grad_b_acc, void* ws,
+                             size_t ws_bytes, lce_stream_t stream, uint32_t flags) {
     Problem pb{N, H, V, X, W, b, y, ignore_index};
     Outputs o;
     memset(&o, 0, sizeof(o));
@@ -550,15 +564,25 @@ lce_status_t lce_backward(int64_t N, int64_t H, int64_t V, const lce_bf16* X, co
     o.grad_b = grad_b;
     o.grad_W_acc = grad_W_acc;
     o.grad_b_acc = grad_b_acc;
+    o.flags = flags;
     return run(pb, o, false, true, chunk_rows, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
-lce_status_t lce_fused_fwd_bwd(int64_t N, int64_t H, int64_t V, const lce_bf16* X, const lce_bf16* W,
-                               const lce_bf16* b, const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
-                               float grad_scale, const float* d_grad_output, float* loss, float* lse,
-                               int64_t* n_valid, lce_bf16* grad_X, lce_bf16* grad_W, lce_bf16* grad_b,
-                               float* grad_W_acc, float* grad_b_acc, void* ws, size_t ws_bytes,
-                               lce_stream_t stream) {
+lce_status_t lce_backward(int64_t N, int64_t H, int64_t V, const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
+                          const int64_t* y, int64_t ignore_index, int64_t chunk_rows, const float* lse,
+                          float grad_scale, const float* d_grad_output, lce_bf16* grad_X, lce_bf16* grad_W,
+                          lce_bf16* grad_b, float* grad_W_acc, float* grad_b_acc, void* ws, size_t ws_bytes,
+                          lce_stream_t stream) {
+    return lce_backward_ex(N, H, V, X, W, b, y, ignore_index, chunk_rows, lse, grad_scale, d_grad_output, grad_X,
+                           grad_W, grad_b, grad_W_acc, grad_b_acc, ws, ws_bytes, stream, 0);
+}
+
+lce_status_t lce_fused_fwd_bwd_ex(int64_t N, int64_t H, int64_t V, const lce_bf16* X, const lce_bf16* W,
+                                  const lce_bf16* b, const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
+                                  float grad_scale, const float* d_grad_output, float* loss, float* lse,
+                                  int64_t* n_valid, lce_bf16* grad_X, lce_bf16* grad_W, lce_bf16* grad_b,
+                                  float* grad_W_acc, float* grad_b_acc, void* ws, size_t ws_bytes,
+                                  lce_stream_t stream, uint32_t flags) {
     Problem pb{N, H, V, X, W, b, y, ignore_index};
     Outputs o;
     memset(&o, 0, sizeof(o));
@@ -572,7 +596,18 @@ lce_status_t lce_fused_fwd_bwd(int64_t N, int64_t H, int64_t V, const lce_bf16* 
     o.grad_b = grad_b;
     o.grad_W_acc = grad_W_acc;
     o.grad_b_acc = grad_b_acc;
+    o.flags = flags;
     return run(pb, o, true, true, chunk_rows, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lce_status_t lce_fused_fwd_bwd(int64_t N, int64_t H, int64_t V, const lce_bf16* X, const lce_bf16* W,
+                               const lce_bf16* b, const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
+                               float grad_scale, const float* d_grad_output, float* loss, float* lse,
+                               int64_t* n_valid, lce_bf16* grad_X, lce_bf16* grad_W, lce_bf16* grad_b,
+                               float* grad_W_acc, float* grad_b_acc, void* ws, size_t ws_bytes,
+                               lce_stream_t stream) {
+    return lce_fused_fwd_bwd_ex(N, H, V, X, W, b, y, ignore_index, chunk_rows, grad_scale, d_grad_output, loss, lse,
+                                n_valid, grad_X, grad_W, grad_b, grad_W_acc, grad_b_acc, ws, ws_bytes, stream, 0);
 }
 
 lce_status_t lce_scale_grads(int64_t N, int64_t H, int64_t V, const float* d_grad_output, lce_bf16* grad_X,

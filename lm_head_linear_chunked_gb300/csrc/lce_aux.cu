@@ -52,10 +52,13 @@ __global__ void prepass_kernel(const int64_t* __restrict__ y, int64_t N, int64_t
 
 // s = grad_scale * grad_output / n_valid (0 without valid rows).
 __global__ void scale_kernel(WsHeader* hdr, float grad_scale, const float* d_grad_output,
-                             int64_t* n_valid_out) {
+                             int64_t* n_valid_out, int sum_reduction) {
     const unsigned long long nv = hdr->n_valid;
     const double go = d_grad_output ? static_cast<double>(*d_grad_output) : 1.0;
-    hdr->scale = nv ? static_cast<float>(static_cast<double>(grad_scale) * go / static_cast<double>(nv)) : 0.f;
+    if (sum_reduction)
+        hdr->scale = static_cast<float>(static_cast<double>(grad_scale) * go);
+    else
+        hdr->scale = nv ? static_cast<float>(static_cast<double>(grad_scale) * go / static_cast<double>(nv)) : 0.f;
     if (n_valid_out) *n_valid_out = static_cast<int64_t>(nv);
 }
 
@@ -263,7 +266,7 @@ __global__ void gather_f16_kernel(const uint16_t* __restrict__ X_chunk, int64_t 
 // loss = sum of row losses / n_valid.  One block; the summation order
 // depends on N only, so the result does not depend on the chunk size.
 __global__ void loss_kernel(const float* __restrict__ row_loss, int64_t N, const WsHeader* hdr,
-                            float* loss, int64_t* n_valid_out) {
+                            float* loss, int64_t* n_valid_out, int sum_reduction) {
     __shared__ double red[1024];
     double acc = 0.0;
     for (int64_t i = threadIdx.x; i < N; i += blockDim.x) acc += static_cast<double>(row_loss[i]);
@@ -275,7 +278,10 @@ __global__ void loss_kernel(const float* __restrict__ row_loss, int64_t N, const
     }
     if (threadIdx.x == 0) {
         const unsigned long long nv = hdr->n_valid;
-        *loss = nv ? static_cast<float>(red[0] / static_cast<double>(nv)) : 0.f;
+        if (sum_reduction)
+            *loss = static_cast<float>(red[0]);
+        else
+            *loss = nv ? static_cast<float>(red[0] / static_cast<double>(nv)) : 0.f;
         if (n_valid_out) *n_valid_out = static_cast<int64_t>(nv);
     }
 }
@@ -655,8 +661,8 @@ cudaError_t launch_onehot_scatter(const unsigned long long* keys, const unsigned
 }
 
 cudaError_t launch_scale(WsHeader* hdr, float grad_scale, const float* d_grad_output, int64_t* n_valid_out,
-                         cudaStream_t s) {
-    scale_kernel<<<1, 1, 0, s>>>(hdr, grad_scale, d_grad_output, n_valid_out);
+                         bool sum_reduction, cudaStream_t s) {
+    scale_kernel<<<1, 1, 0, s>>>(hdr, grad_scale, d_grad_output, n_valid_out, sum_reduction ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -671,8 +677,8 @@ cudaError_t launch_combine(const float* part_m, const float* part_s, int64_t n_p
 }
 
 cudaError_t launch_loss(const float* row_loss, int64_t N, const WsHeader* hdr, float* loss, int64_t* n_valid_out,
-                        cudaStream_t s) {
-    loss_kernel<<<1, 1024, 0, s>>>(row_loss, N, hdr, loss, n_valid_out);
+                        bool sum_reduction, cudaStream_t s) {
+    loss_kernel<<<1, 1024, 0, s>>>(row_loss, N, hdr, loss, n_valid_out, sum_reduction ? 1 : 0);
     return cudaGetLastError();
 }
 

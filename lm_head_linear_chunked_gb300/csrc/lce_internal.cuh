@@ -191,13 +191,15 @@ cudaError_t launch_onehot_scatter(const unsigned long long* keys, const unsigned
                                   const int* run_count, const uint16_t* X_chunk, int64_t H,
                                   const WsHeader* hdr, float* grad_W_acc, uint16_t* grad_W,
                                   int write_bf16, int grid, cudaStream_t s);
+// s = grad_scale * grad_output / n_valid (mean), or grad_scale * grad_output (sum_reduction).
 cudaError_t launch_scale(WsHeader* hdr, float grad_scale, const float* d_grad_output,
-                         int64_t* n_valid_out, cudaStream_t s);
+                         int64_t* n_valid_out, bool sum_reduction, cudaStream_t s);
 cudaError_t launch_combine(const float* part_m, const float* part_s, int64_t n_vt, int64_t ldp,
                            int64_t rows, const float* zt, const int64_t* y, int64_t ignore_index,
                            float* lse, float* row_loss, cudaStream_t s);
+// loss = mean (or, with sum_reduction, sum) of the row losses of the valid rows.
 cudaError_t launch_loss(const float* row_loss, int64_t N, const WsHeader* hdr, float* loss,
-                        int64_t* n_valid_out, cudaStream_t s);
+                        int64_t* n_valid_out, bool sum_reduction, cudaStream_t s);
 cudaError_t launch_grad_b(const float* gb_part, int64_t parts, int64_t V, const WsHeader* hdr,
                           const int* label_counts, float* grad_b_acc, uint16_t* grad_b, int first,
                           int last, cudaStream_t s);

@@ -151,3 +151,30 @@ def test_profile_end_without_begin_is_empty():
     out = lce.lce_profile_end()
     assert set(out) == set(lce.PROFILE_KINDS)
     assert all(v == (0.0, 0) for v in out.values())
+
+
+@pytest.mark.parametrize("flags", [lce.ACCUMULATE, 4, 1 << 31])
+def test_forward_ex_rejects_flags(flags):
+    # accumulate has no meaning without gradients; unknown bits are errors
+    args = dict(N=16, H=64, V=32, X=A, W=A, b=None, y=A, ignore_index=-100, chunk_rows=0, loss=A, lse=A,
+                n_valid=None, ws=A, ws_bytes=1 << 30, stream=None, flags=flags)
+    with pytest.raises(lce.LCEError) as e:
+        lce.lce_forward_ex(*args.values())
+    assert e.value.status == 1
+
+
+@pytest.mark.parametrize("flags", [4, 8 | lce.REDUCTION_SUM])
+def test_backward_ex_rejects_unknown_flags(flags):
+    args = dict(N=16, H=64, V=32, X=A, W=A, b=None, y=A, ignore_index=-100, chunk_rows=0, lse=A, grad_scale=1.0,
+                d_grad_output=None, grad_X=A, grad_W=A, grad_b=None, grad_W_acc=A, grad_b_acc=None, ws=A,
+                ws_bytes=1 << 30, stream=None, flags=flags)
+    with pytest.raises(lce.LCEError) as e:
+        lce.lce_backward_ex(*args.values())
+    assert e.value.status == 1
+
+
+def test_reduction_names_are_checked():
+    assert lce._flags("sum", True) == lce.REDUCTION_SUM | lce.ACCUMULATE
+    assert lce._flags("mean", False) == 0
+    with pytest.raises(ValueError):
+        lce._flags("none", False)
