@@ -51,12 +51,12 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # they were captured with: DRAM_BYTES_SOURCES lists the files that decide a
 # GEMM launch's traffic and DRAM_BYTES_DIGEST their SHA-256 at capture time.
 # When the digest no longer matches, roofline.traffic is reported as null.
-DRAM_BYTES_PER_LAUNCH = {"grad_w": 25.57e9 + 2.47e9, "grad_x": 31.70e9 + 0.13e9,
-                         "logits_lse": 5.21e9 + 4.87e9, "recomputed_logits_softmax": None}
+DRAM_BYTES_PER_LAUNCH = {"grad_w": 42.15e9 + 2.49e9, "grad_x": 62.14e9 + 0.13e9,
+                         "logits_lse": 15.24e9 + 4.89e9, "recomputed_logits_softmax": None}
 DRAM_BYTES_CHUNK_ROWS = 16384  # the chunk size those launches ran with
 DRAM_BYTES_SOURCES = ["csrc/lce_gemm.cuh", "csrc/lce_internal.cuh", "csrc/lce_ptx.cuh", "csrc/lce_api.cu",
                       "csrc/lce_gemm_logits.cu", "csrc/lce_gemm_grads.cu"]
-DRAM_BYTES_DIGEST = "5a4a9d574f319420"
+DRAM_BYTES_DIGEST = "ef97b5d5d9a2550e"
 
 
 def gemm_source_digest() -> str:
