@@ -85,8 +85,15 @@ typedef enum {
     LCE_ERR_CUDA = 6           /* a CUDA runtime call or launch failed */
 } lce_status_t;
 
-/* Which entry point a workspace is sized for. */
-enum { LCE_WS_FORWARD = 0, LCE_WS_BACKWARD = 1, LCE_WS_FUSED = 2 };
+/* Which entry point a workspace is sized for.  LCE_WS_FUSED is the size for
+ * the fused call's fastest schedule: with chunks of at least 4096 rows, no
+ * bias and two or more chunks, it holds two chunks of the kept fp16
+ * exponentials, so that each chunk's forward also turns the previous
+ * chunk's into the softmax while its tensor cores work.  LCE_WS_FUSED_MIN
+ * is the smallest workspace the fused call accepts; with less than the
+ * LCE_WS_FUSED size it runs the two steps one after the other (same
+ * results). */
+enum { LCE_WS_FORWARD = 0, LCE_WS_BACKWARD = 1, LCE_WS_FUSED = 2, LCE_WS_FUSED_MIN = 3 };
 
 /* Bytes of workspace the entry point `which` needs for this problem.
  * Host only; enqueues nothing.  Writes *bytes on LCE_OK. */

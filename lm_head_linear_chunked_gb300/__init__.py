@@ -20,7 +20,7 @@ import threading
 from typing import Optional
 
 __all__ = [
-    "LCEError", "IGNORE_INDEX", "WS_FORWARD", "WS_BACKWARD", "WS_FUSED", "STATUS", "library_path", "lib",
+    "LCEError", "IGNORE_INDEX", "WS_FORWARD", "WS_BACKWARD", "WS_FUSED", "WS_FUSED_MIN", "STATUS", "library_path", "lib",
     "lce_workspace_size", "lce_chunk_rows", "lce_forward", "lce_backward", "lce_fused_fwd_bwd",
     "lce_check_status", "lce_status_string", "lce_debug_gemm", "lce_debug_wait_timeout",
     "lce_profile_begin", "lce_profile_end", "PROFILE_KINDS", "lce_forward_static_ws", "STATIC_SCRATCH_BYTES",
@@ -29,7 +29,7 @@ __all__ = [
 ]
 
 IGNORE_INDEX = -100
-WS_FORWARD, WS_BACKWARD, WS_FUSED = 0, 1, 2
+WS_FORWARD, WS_BACKWARD, WS_FUSED, WS_FUSED_MIN = 0, 1, 2, 3
 STATUS = {0: "LCE_OK", 1: "LCE_ERR_INVALID_ARG", 2: "LCE_ERR_UNSUPPORTED", 3: "LCE_ERR_WORKSPACE",
           4: "LCE_ERR_LABEL_RANGE", 5: "LCE_ERR_TIMEOUT", 6: "LCE_ERR_CUDA"}
 

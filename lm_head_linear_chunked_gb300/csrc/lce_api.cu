@@ -17,6 +17,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 constexpr int64_t AUTO_CHUNK_ROWS = 16384;
+// Smallest chunk whose forward hides the previous chunk's softmax rescale.
+constexpr int64_t OVERLAP_MIN_ROWS = 4096;
 // Tile-order groups: 4096 rows of X (32 MB at H = 4096) for the logits
 // passes, 2048 rows of P for grad_X; for the grad_W pass, as many 256-column tiles of the
 // fp16 X chunk as make about 32 MB (8 at 8192 rows, 4 at 16384).
@@ -50,8 +52,11 @@ constexpr size_t HEADER_BYTES = 1024;
 struct Plan {
     int64_t N, H, V, C, n_chunks, n_vt, ldg, mt_chunk, label_blocks_per_chunk, gradx_splits;
     bool has_bias;
+    // fused call: chunk c's forward rescales chunk c-1's E (two E and two
+    // half-tile-max buffers)
+    bool overlap;
     size_t off_row_loss, off_zt, off_pm, off_ps, off_g, off_gb, off_keys, off_runs, off_nrun, off_counts, off_w16,
-        off_x16, off_dmap, off_crow, off_nvc, off_split, total;
+        off_x16, off_dmap, off_crow, off_nvc, off_split, off_g2, off_pm2, total;
 };
 
 lce_status_t check_sizes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows) {
@@ -69,7 +74,7 @@ lce_status_t make_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, bool
                        Plan* p) {
     lce_status_t st = check_sizes(N, H, V, chunk_rows);
     if (st != LCE_OK) return st;
-    if (which < LCE_WS_FORWARD || which > LCE_WS_FUSED) return LCE_ERR_INVALID_ARG;
+    if (which < LCE_WS_FORWARD || which > LCE_WS_FUSED_MIN) return LCE_ERR_INVALID_ARG;
     p->N = N;
     p->H = H;
     p->V = V;
@@ -81,7 +86,11 @@ lce_status_t make_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, bool
     p->label_blocks_per_chunk = cdiv(p->C, LABEL_BLOCK);
     p->gradx_splits = gradx_splits(p->C, H, V);
     p->has_bias = has_bias;
-    const bool fwd = which != LCE_WS_BACKWARD, bwd = which != LCE_WS_FORWARD;
+    // Overlap only where a chunk's forward is long enough to hide the
+    // previous chunk's rescale; the bias case keeps the rescale kernel, which
+    // also sums P's columns for grad_b.
+    p->overlap = which == LCE_WS_FUSED && !has_bias && p->n_chunks >= 2 && p->C >= OVERLAP_MIN_ROWS;
+    const bool fwd = which != LCE_WS_BACKWARD, bwd = which != LCE_WS_FORWARD;  // FUSED_MIN: both
     size_t off = HEADER_BYTES;
     auto take = [&](bool use, size_t bytes) -> size_t {
         if (!use) return 0;
@@ -105,6 +114,8 @@ lce_status_t make_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, bool
     p->off_crow = take(bwd, static_cast<size_t>(N) * 4);
     p->off_nvc = take(bwd, static_cast<size_t>(p->n_chunks) * 4);
     p->off_split = take(bwd && p->gradx_splits > 1, static_cast<size_t>(p->gradx_splits) * p->C * H * 4);
+    p->off_g2 = take(p->overlap, static_cast<size_t>(p->C) * p->ldg * 2);
+    p->off_pm2 = take(p->overlap, static_cast<size_t>(2 * p->n_vt) * p->C * 4);
     p->total = off;
     return LCE_OK;
 }
@@ -287,6 +298,13 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     const int which = do_fwd && do_bwd ? LCE_WS_FUSED : (do_fwd ? LCE_WS_FORWARD : LCE_WS_BACKWARD);
     lce_status_t st = make_plan(pb.N, pb.H, pb.V, chunk_rows, pb.b != nullptr, which, &p);
     if (st != LCE_OK) return st;
+    // The fused call overlaps each chunk's softmax rescale with the next
+    // chunk's forward when the workspace holds the second chunk of E, and
+    // runs them one after the other when it holds only the minimum.
+    if (which == LCE_WS_FUSED && ws_bytes < p.total) {
+        st = make_plan(pb.N, pb.H, pb.V, chunk_rows, pb.b != nullptr, LCE_WS_FUSED_MIN, &p);
+        if (st != LCE_OK) return st;
+    }
     // pointer checks
     if (!pb.X || !pb.W || !pb.y || !ws || !o.lse) return LCE_ERR_INVALID_ARG;
     if (!aligned16(pb.X) || !aligned16(pb.W) || !aligned16(pb.b) || !aligned16(pb.y) || !aligned16(o.lse) ||
@@ -328,6 +346,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     int* nvc = do_bwd ? reinterpret_cast<int*>(wsb + p.off_nvc) : nullptr;    // valid rows per chunk
     float* split_out = (do_bwd && p.gradx_splits > 1) ? reinterpret_cast<float*>(wsb + p.off_split) : nullptr;
     int* counts = (do_bwd && pb.b) ? reinterpret_cast<int*>(wsb + p.off_counts) : nullptr;
+    uint16_t* G2 = p.overlap ? reinterpret_cast<uint16_t*>(wsb + p.off_g2) : nullptr;
+    float* pm2 = p.overlap ? reinterpret_cast<float*>(wsb + p.off_pm2) : nullptr;
 
     // operand maps of the whole X and W
     CUtensorMap mX_k, mW_k, mW16_mn;
@@ -355,12 +375,62 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
         if (o.grad_X) LCE_LAUNCH(PK_OTHER, launch_zero_ignored_rows(dmap, pb.N, pb.H, o.grad_X, s));
     }
 
-    for (int64_t c = 0; c < p.n_chunks; ++c) {
+    // The forward of chunk c (logits, logsumexp, and in the fused call E kept
+    // in Gc), with the previous chunk's rescale as its side job when side >= 0.
+    auto forward_chunk = [&](int64_t c, uint16_t* Gc, float* pmc, int64_t side) -> lce_status_t {
         const int64_t r0 = c * p.C;
         const int64_t rows = (pb.N - r0) < p.C ? (pb.N - r0) : p.C;
         const int64_t mt = cdiv(rows, BM);        // 128-row tiles (grad_b partial rows)
         const int64_t mtf = cdiv(rows, form.rows);  // tiles of the GEMM form
-        if (do_fwd) {
+        (void)mt;
+        GemmArgs a = base_args(hdr);
+        a.m_tiles = static_cast<int32_t>(mtf);
+        a.n_tiles = static_cast<int32_t>(p.n_vt);
+        a.k_blocks = static_cast<int32_t>(cdiv(pb.H, BK));
+        a.raster = 2;
+        a.group_m = static_cast<int32_t>(LOGITS_GROUP_ROWS / form.rows);
+        a.a_y0 = static_cast<int32_t>(r0);
+        a.M = rows;
+        a.N = pb.V;
+        a.y = pb.y + r0;
+        a.ignore_index = pb.ignore_index;
+        a.bias = pb.b;
+        a.part_m = pmc;
+        a.part_s = ps;
+        a.zt = zt;
+        a.ldp = p.C;
+        if (do_bwd) {  // keep E = 2^(t - tile max) of the valid rows for the backward: no recompute
+            a.g = Gc;
+            a.ldg = p.ldg;
+            a.row_map = dmap + r0;
+        }
+        if (side >= 0) {  // the epilogue warps rescale the previous chunk's E meanwhile
+            const int64_t sr0 = side * p.C;
+            a.side_p = (side & 1) ? G2 : G;
+            a.side_pm = (side & 1) ? pm2 : pm;
+            a.side_lse = o.lse + sr0;
+            a.side_crow = crow + sr0;
+            a.side_nvalid = nvc + side;
+            a.side_rows = (pb.N - sr0) < p.C ? (pb.N - sr0) : p.C;
+        }
+        LCE_LAUNCH(PK_LSE, launch_gemm(MODE_LSE, mX_k, mW_k, mW_k, a, grid_of(form, mtf * p.n_vt), s, form.pair));
+        LCE_LAUNCH(PK_OTHER, launch_combine(pmc, ps, 2 * p.n_vt, p.C, rows, zt, pb.y + r0, pb.ignore_index,
+                                            o.lse + r0, row_loss + r0, s));
+        return LCE_OK;
+    };
+    // The backward of chunk c; `rescaled`: its E was already turned into P.
+    auto backward_chunk = [&](int64_t c, uint16_t* Gc, const float* pmc, bool rescaled) -> lce_status_t {
+        const int64_t r0 = c * p.C;
+        const int64_t rows = (pb.N - r0) < p.C ? (pb.N - r0) : p.C;
+        const int64_t mt = cdiv(rows, BM);        // 128-row tiles (grad_b partial rows)
+        const int64_t mtf = cdiv(rows, form.rows);  // tiles of the GEMM form
+        // first: the chunk that overwrites the FP32 accumulators (none when accumulating)
+        const bool first = c == 0 && !accumulate, last = c == p.n_chunks - 1;
+        if (do_fwd) {  // P = E 2^(tile max - lse), in place (unless the next forward did it)
+            if (!rescaled)
+                LCE_LAUNCH(PK_OTHER, launch_p_rescale(Gc, p.ldg, rows, pb.V, pmc, p.C, o.lse + r0, crow + r0,
+                                                      nvc + c, gb, s));
+        } else {   // recompute the logits; P = softmax (fp16)
             GemmArgs a = base_args(hdr);
             a.m_tiles = static_cast<int32_t>(mtf);
             a.n_tiles = static_cast<int32_t>(p.n_vt);
@@ -373,120 +443,112 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             a.y = pb.y + r0;
             a.ignore_index = pb.ignore_index;
             a.bias = pb.b;
-            a.part_m = pm;
-            a.part_s = ps;
-            a.zt = zt;
-            a.ldp = p.C;
-            if (do_bwd) {  // keep E = 2^(t - tile max) of the valid rows for the backward: no recompute
-                a.g = G;
-                a.ldg = p.ldg;
-                a.row_map = dmap + r0;
-            }
-            LCE_LAUNCH(PK_LSE, launch_gemm(MODE_LSE, mX_k, mW_k, mW_k, a, grid_of(form, mtf * p.n_vt), s, form.pair));
-            LCE_LAUNCH(PK_OTHER, launch_combine(pm, ps, 2 * p.n_vt, p.C, rows, zt, pb.y + r0, pb.ignore_index, o.lse + r0,
-                                        row_loss + r0, s));
+            a.lse = o.lse + r0;
+            a.g = Gc;
+            a.ldg = p.ldg;
+            a.gb_part = gb;
+            a.row_map = dmap + r0;
+            LCE_LAUNCH(PK_P, launch_gemm(MODE_G, mX_k, mW_k, mW_k, a, grid_of(form, mtf * p.n_vt), s, form.pair));
         }
-        if (do_bwd) {
-            // first: the chunk that overwrites the FP32 accumulators (none when accumulating)
-            const bool first = c == 0 && !accumulate, last = c == p.n_chunks - 1;
-            if (do_fwd) {  // P = E 2^(tile max - lse), in place
-                LCE_LAUNCH(PK_OTHER, launch_p_rescale(G, p.ldg, rows, pb.V, pm, p.C, o.lse + r0, crow + r0, nvc + c,
-                                                      gb, s));
-            } else {   // recompute the logits; P = softmax (fp16)
-                GemmArgs a = base_args(hdr);
-                a.m_tiles = static_cast<int32_t>(mtf);
-                a.n_tiles = static_cast<int32_t>(p.n_vt);
-                a.k_blocks = static_cast<int32_t>(cdiv(pb.H, BK));
-                a.raster = 2;
-                a.group_m = static_cast<int32_t>(LOGITS_GROUP_ROWS / form.rows);
-                a.a_y0 = static_cast<int32_t>(r0);
-                a.M = rows;
-                a.N = pb.V;
-                a.y = pb.y + r0;
-                a.ignore_index = pb.ignore_index;
-                a.bias = pb.b;
-                a.lse = o.lse + r0;
-                a.g = G;
-                a.ldg = p.ldg;
-                a.gb_part = gb;
-                a.row_map = dmap + r0;
-                LCE_LAUNCH(PK_P, launch_gemm(MODE_G, mX_k, mW_k, mW_k, a, grid_of(form, mtf * p.n_vt), s, form.pair));
-            }
-            if (gb)
-                LCE_LAUNCH(PK_OTHER, launch_grad_b(gb, mt * 4, pb.V, hdr, counts, o.grad_b_acc, o.grad_b, first, last, s));
-            // P and X_c maps bounded to this chunk's rows: rows past it read as zero
-            LCE_LAUNCH(PK_OTHER, launch_gather_f16(pb.X + r0 * pb.H, pb.H, crow + r0, nvc + c, rows, &hdr->amax_x_bits,
-                                                   X16, do_fwd ? nullptr : G, p.ldg, s));
-            CUtensorMap mG_k, mG_mn, mX16_mn;
-            if (!map_16bit_2d(&mG_k, G, rows, pb.V, p.ldg, 64, BM, true) ||
-                !map_16bit_2d(&mG_mn, G, rows, pb.V, p.ldg, 64, 64, true) ||
-                !map_16bit_2d(&mX16_mn, X16, rows, pb.H, pb.H, 64, 64, true))
-                return LCE_ERR_CUDA;
-            if (o.grad_X) {   // grad_X_c = s (P W - W[y])
-                GemmArgs a = base_args(hdr);
-                a.m_tiles = static_cast<int32_t>(mtf);
-                a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
-                a.k_blocks = static_cast<int32_t>(cdiv(pb.V, BK));
-                a.raster = 2;
-                a.group_m = static_cast<int32_t>(GRADX_GROUP_ROWS / form.rows);
-                a.M = rows;
-                a.N = pb.H;
-                a.scale = &hdr->scale;
-                a.out_bf16 = o.grad_X + r0 * pb.H;
-                a.ld_out = pb.H;
-                a.y = pb.y + r0;
-                a.ignore_index = pb.ignore_index;
-                a.w_rows = pb.W;
-                a.ldw = pb.H;
-                a.V = pb.V;
-                a.b_amax_bits = &hdr->amax_w_bits;
-                a.row_map = crow + r0;
-                a.dyn_rows = nvc + c;
-                a.k_splits = static_cast<int32_t>(p.gradx_splits);
-                a.k_per_split = static_cast<int32_t>(cdiv(a.k_blocks, p.gradx_splits));
-                a.split_out = split_out;
-                a.split_stride = p.C * pb.H;
-                LCE_LAUNCH(PK_GRADX, launch_gemm(MODE_GRADX, mG_k, mW16_mn, mW16_mn, a,
-                                                 grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles *
-                                                                   p.gradx_splits),
-                                                 s, form.pair));
-                if (split_out)
-                    LCE_LAUNCH(PK_GRADX, launch_gradx_split_reduce(split_out, p.gradx_splits, p.C * pb.H, pb.H, crow + r0,
-                                                                   nvc + c, rows, pb.y + r0, pb.ignore_index, pb.V,
-                                                                   pb.W, hdr, o.grad_X + r0 * pb.H, s));
-            }
-            {   // grad_W_acc (+)= s P^T X_c
-                GemmArgs a = base_args(hdr);
-                a.m_tiles = static_cast<int32_t>(cdiv(pb.V, form.rows));
-                a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
-                a.k_blocks = static_cast<int32_t>(cdiv(rows, BK));
-                a.raster = 3;
-                a.group_n = gradw_group_n(rows);
-                a.M = pb.V;
-                a.N = pb.H;
-                a.scale = &hdr->scale;
-                a.out_f32 = o.grad_W_acc;
-                a.ld_f32 = pb.H;
-                a.out_bf16 = o.grad_W;
-                a.ld_out = pb.H;
-                a.acc_first = first;
-                a.write_bf16 = last && o.grad_W != nullptr;
-                a.acc_tma = 1;
-                a.b_amax_bits = &hdr->amax_x_bits;
-                a.dyn_rows = nvc + c;
-                LCE_LAUNCH(PK_GRADW, launch_gemm(MODE_GRADW, mG_mn, mX16_mn, mAcc, a,
-                                                 grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles), s,
-                                                 form.pair));
-            }
-            // grad_W_acc[y_i] -= s X[i] for the chunk's valid rows, exactly, in row order
-            for (int64_t k = 0; k < p.label_blocks_per_chunk; ++k) {
-                if (rows - k * LABEL_BLOCK <= 0) break;
-                const int64_t blk = c * p.label_blocks_per_chunk + k;
-                LCE_LAUNCH(PK_OTHER, launch_onehot_scatter(keys + blk * LABEL_BLOCK, runs + blk * LABEL_BLOCK,
-                                                           nrun + blk, pb.X + r0 * pb.H, pb.H, hdr, o.grad_W_acc,
-                                                           o.grad_W, last && o.grad_W != nullptr, 4 * sm_count(), s));
-            }
+        if (gb)
+            LCE_LAUNCH(PK_OTHER, launch_grad_b(gb, mt * 4, pb.V, hdr, counts, o.grad_b_acc, o.grad_b, first, last, s));
+        // P and X_c maps bounded to this chunk's rows: rows past it read as zero
+        LCE_LAUNCH(PK_OTHER, launch_gather_f16(pb.X + r0 * pb.H, pb.H, crow + r0, nvc + c, rows, &hdr->amax_x_bits,
+                                               X16, do_fwd ? nullptr : Gc, p.ldg, s));
+        CUtensorMap mG_k, mG_mn, mX16_mn;
+        if (!map_16bit_2d(&mG_k, Gc, rows, pb.V, p.ldg, 64, BM, true) ||
+            !map_16bit_2d(&mG_mn, Gc, rows, pb.V, p.ldg, 64, 64, true) ||
+            !map_16bit_2d(&mX16_mn, X16, rows, pb.H, pb.H, 64, 64, true))
+            return LCE_ERR_CUDA;
+        if (o.grad_X) {   // grad_X_c = s (P W - W[y])
+            GemmArgs a = base_args(hdr);
+            a.m_tiles = static_cast<int32_t>(mtf);
+            a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
+            a.k_blocks = static_cast<int32_t>(cdiv(pb.V, BK));
+            a.raster = 2;
+            a.group_m = static_cast<int32_t>(GRADX_GROUP_ROWS / form.rows);
+            a.M = rows;
+            a.N = pb.H;
+            a.scale = &hdr->scale;
+            a.out_bf16 = o.grad_X + r0 * pb.H;
+            a.ld_out = pb.H;
+            a.y = pb.y + r0;
+            a.ignore_index = pb.ignore_index;
+            a.w_rows = pb.W;
+            a.ldw = pb.H;
+            a.V = pb.V;
+            a.b_amax_bits = &hdr->amax_w_bits;
+            a.row_map = crow + r0;
+            a.dyn_rows = nvc + c;
+            a.k_splits = static_cast<int32_t>(p.gradx_splits);
+            a.k_per_split = static_cast<int32_t>(cdiv(a.k_blocks, p.gradx_splits));
+            a.split_out = split_out;
+            a.split_stride = p.C * pb.H;
+            LCE_LAUNCH(PK_GRADX, launch_gemm(MODE_GRADX, mG_k, mW16_mn, mW16_mn, a,
+                                             grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles *
+                                                               p.gradx_splits),
+                                             s, form.pair));
+            if (split_out)
+                LCE_LAUNCH(PK_GRADX, launch_gradx_split_reduce(split_out, p.gradx_splits, p.C * pb.H, pb.H, crow + r0,
+                                                               nvc + c, rows, pb.y + r0, pb.ignore_index, pb.V,
+                                                               pb.W, hdr, o.grad_X + r0 * pb.H, s));
         }
+        {   // grad_W_acc (+)= s P^T X_c
+            GemmArgs a = base_args(hdr);
+            a.m_tiles = static_cast<int32_t>(cdiv(pb.V, form.rows));
+            a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
+            a.k_blocks = static_cast<int32_t>(cdiv(rows, BK));
+            a.raster = 3;
+            a.group_n = gradw_group_n(rows);
+            a.M = pb.V;
+            a.N = pb.H;
+            a.scale = &hdr->scale;
+            a.out_f32 = o.grad_W_acc;
+            a.ld_f32 = pb.H;
+            a.out_bf16 = o.grad_W;
+            a.ld_out = pb.H;
+            a.acc_first = first;
+            a.write_bf16 = last && o.grad_W != nullptr;
+            a.acc_tma = 1;
+            a.b_amax_bits = &hdr->amax_x_bits;
+            a.dyn_rows = nvc + c;
+            LCE_LAUNCH(PK_GRADW, launch_gemm(MODE_GRADW, mG_mn, mX16_mn, mAcc, a,
+                                             grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles), s,
+                                             form.pair));
+        }
+        // grad_W_acc[y_i] -= s X[i] for the chunk's valid rows, exactly, in row order
+        for (int64_t k = 0; k < p.label_blocks_per_chunk; ++k) {
+            if (rows - k * LABEL_BLOCK <= 0) break;
+            const int64_t blk = c * p.label_blocks_per_chunk + k;
+            LCE_LAUNCH(PK_OTHER, launch_onehot_scatter(keys + blk * LABEL_BLOCK, runs + blk * LABEL_BLOCK,
+                                                       nrun + blk, pb.X + r0 * pb.H, pb.H, hdr, o.grad_W_acc,
+                                                       o.grad_W, last && o.grad_W != nullptr, 4 * sm_count(), s));
+        }
+        return LCE_OK;
+    };
+
+    // With p.overlap, chunk c's forward runs before chunk c-1's backward and
+    // rescales chunk c-1's E meanwhile; E and the half-tile maxes alternate
+    // between two buffers.
+    for (int64_t c = 0; c < p.n_chunks; ++c) {
+        uint16_t* Gc = (p.overlap && (c & 1)) ? G2 : G;
+        float* pmc = (p.overlap && (c & 1)) ? pm2 : pm;
+        if (do_fwd) {
+            st = forward_chunk(c, Gc, pmc, p.overlap && c >= 1 ? c - 1 : -1);
+            if (st != LCE_OK) return st;
+        }
+        if (do_bwd && !p.overlap) {
+            st = backward_chunk(c, Gc, pmc, false);
+            if (st != LCE_OK) return st;
+        } else if (do_bwd && c >= 1) {
+            st = backward_chunk(c - 1, ((c - 1) & 1) ? G2 : G, ((c - 1) & 1) ? pm2 : pm, true);
+            if (st != LCE_OK) return st;
+        }
+    }
+    if (do_bwd && p.overlap) {
+        const int64_t c = p.n_chunks - 1;
+        st = backward_chunk(c, (c & 1) ? G2 : G, (c & 1) ? pm2 : pm, false);
+        if (st != LCE_OK) return st;
     }
     if (do_fwd) LCE_LAUNCH(PK_OTHER, launch_loss(row_loss, pb.N, hdr, o.loss, o.n_valid, sum_reduction, s));
     return LCE_OK;

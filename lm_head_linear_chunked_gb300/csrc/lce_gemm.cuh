@@ -209,6 +209,73 @@ __device__ __forceinline__ void gradw_load_old(const GemmArgs& a, int64_t row_ba
     }
 }
 
+// The previous chunk's softmax rescale as a side job of the forward's
+// epilogue warps (GemmArgs::side_p): P = fp16(E * 2^(half-tile max - lse
+// log2 e)) in place, rows past the compact row count zeroed up to the next
+// multiple of 64, exactly as p_rescale_kernel computes it.  Unit u covers
+// compact rows 8 (u / n_tiles) .. +8 of vocab tile u % n_tiles; the units
+// are dealt round-robin to all epilogue warps of the grid, and each warp
+// works off `budget` of its units after each tile, the rest at the end.
+struct SideJob {
+    int64_t next, stride, units, nv, zero_end;
+    int budget;
+};
+
+__device__ __forceinline__ void side_init(const GemmArgs& a, SideJob& j, int64_t gwarp, int64_t nwarps,
+                                          int64_t tiles_here) {
+    j.next = gwarp;
+    j.stride = nwarps;
+    j.units = 0;
+    j.budget = 0;
+    if (!a.side_p) return;
+    j.nv = *a.side_nvalid;
+    j.zero_end = min64((j.nv + 63) / 64 * 64, a.side_rows);
+    j.units = (j.zero_end + 7) / 8 * a.n_tiles;
+    const int64_t mine = (j.units + nwarps - 1) / nwarps;
+    j.budget = static_cast<int>(mine / (tiles_here > 0 ? tiles_here : 1)) + 1;
+}
+
+__device__ __forceinline__ void side_unit(const GemmArgs& a, const SideJob& j, int64_t u, int lane) {
+    const int64_t tile = u % a.n_tiles, rb = u / a.n_tiles;
+    const int64_t c = tile * 256 + lane * 8;
+    if (c >= a.ldg) return;
+    const float* pm = a.side_pm + (2 * tile + (lane >> 4)) * a.ldp;  // one max per 128-column half tile
+    float f[8];
+    uint4 w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t r8 = rb * 8 + i;
+        f[i] = 0.f;
+        if (r8 < j.nv) {
+            const int64_t r = a.side_crow[r8];  // chunk row
+            f[i] = exp2f(pm[r] - a.side_lse[r] * LOG2E_F);
+            w[i] = *reinterpret_cast<const uint4*>(a.side_p + r8 * a.ldg + c);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t r8 = rb * 8 + i;
+        if (r8 >= j.zero_end) break;
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (r8 < j.nv) {
+            const uint32_t in[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+            uint32_t out[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 e = __half22float2(*reinterpret_cast<const __half2*>(&in[k]));
+                __half2 h = __floats2half2_rn(e.x * f[i], e.y * f[i]);
+                out[k] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            o = make_uint4(out[0], out[1], out[2], out[3]);
+        }
+        *reinterpret_cast<uint4*>(a.side_p + r8 * a.ldg + c) = o;
+    }
+}
+
+__device__ __forceinline__ void side_work(const GemmArgs& a, SideJob& j, int lane, int64_t budget) {
+    for (int64_t k = 0; k < budget && j.next < j.units; ++k, j.next += j.stride) side_unit(a, j, j.next, lane);
+}
+
 // Hands an accumulator back to the MMA issuer once a warp has read it: a
 // local arrive, or in the pair form an arrive on rank 0's barrier (given by
 // its cluster address).
@@ -652,6 +719,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int q = warp & 3;
         const int half = (warp - 2) >> 2;
         uint32_t acc = 0, acc_phase = 0;
+        SideJob side;
+        if constexpr (MODE == MODE_LSE)
+            side_init(args, side, static_cast<int64_t>(blockIdx.x) * EPI_WARPS + (warp - 2),
+                      static_cast<int64_t>(gridDim.x) * EPI_WARPS, (num_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x);
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             int m, n, ks;
             tile_and_slice(t, args, m, n, ks);
@@ -672,7 +743,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                 kb1 <= kb0, ks, pre, epi_stage, &map_c);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
+            if constexpr (MODE == MODE_LSE) side_work(args, side, lane, side.budget);
         }
+        if constexpr (MODE == MODE_LSE) side_work(args, side, lane, side.units);
     }
 
     __syncwarp();  // reconverge the producer and MMA warps (one lane worked)

@@ -249,6 +249,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         const int q = warp & 3;
         const int half = (warp - 2) >> 2;
         uint32_t acc = 0, acc_phase = 0;
+        SideJob side;
+        if constexpr (MODE == MODE_LSE)
+            side_init(args, side, static_cast<int64_t>(blockIdx.x) * EPI_WARPS + (warp - 2),
+                      static_cast<int64_t>(gridDim.x) * EPI_WARPS, (num_tiles - cid + ncl - 1) / ncl);
         for (int t = cid; t < num_tiles; t += ncl) {
             int m, n, ks;
             tile_and_slice(t, args, m, n, ks);
@@ -271,7 +275,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                                       pre, epi_stage, &map_c);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
+            if constexpr (MODE == MODE_LSE) side_work(args, side, lane, side.budget);
         }
+        if constexpr (MODE == MODE_LSE) side_work(args, side, lane, side.units);
     }
 
     __syncwarp();  // reconverge the producer and MMA warps (one lane worked)

@@ -159,6 +159,17 @@ struct GemmArgs {
     int32_t k_per_split;
     float* split_out;
     int64_t split_stride;
+    // MODE_LSE side job (fused call): between tiles, the epilogue warps turn
+    // the previous chunk's kept exponentials E into P in place, the work of
+    // p_rescale_kernel, in units of 8 compact rows x one 256-column vocab
+    // tile.  side_p == nullptr: no side job.  n_tiles, ldp, ldg and V are the
+    // current chunk's, which the previous chunk shares.
+    uint16_t* side_p;          // the previous chunk's E [compact rows, ldg]
+    const float* side_pm;      // its [2 n_tiles, ldp] half-tile maxes
+    const float* side_lse;     // lse of its first row
+    const int* side_crow;      // its compact row -> chunk row
+    const int* side_nvalid;    // its number of compact rows (device)
+    int64_t side_rows;         // its number of chunk rows
     unsigned* status;
     uint64_t timeout_ns;
 };

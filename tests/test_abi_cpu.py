@@ -55,12 +55,21 @@ def test_workspace_sizes():
     f = lce.lce_workspace_size(N, H, V, 0, False, lce.WS_FORWARD)
     b = lce.lce_workspace_size(N, H, V, 0, False, lce.WS_BACKWARD)
     fb = lce.lce_workspace_size(N, H, V, 0, False, lce.WS_FUSED)
-    assert fb >= max(f, b) and fb <= f + b
-    assert b >= 16384 * V * 2                      # one chunk of fp16 P
-    assert fb < N * V * 2 / 5                      # far below the logits it replaces
+    C, ldg, n_vt = 16384, V, -(-V // 256)
+    second = C * ldg * 2 + 2 * n_vt * C * 4        # the overlapped chunk's E and half-tile maxes
+    assert fb >= max(f, b) and fb <= f + b + second
+    assert b >= C * V * 2                          # one chunk of fp16 P
+    assert fb < N * V * 2 / 3                      # far below the logits it replaces
     with_bias = lce.lce_workspace_size(N, H, V, 0, True, lce.WS_FUSED)
-    assert with_bias > fb
+    assert with_bias > b                           # no overlap with a bias: one E buffer
+    assert with_bias < fb
     assert lce.lce_workspace_size(N, H, V, 256, False, lce.WS_FUSED) < fb
+    # the fused call's minimum: one chunk of E, no overlap
+    fmin = lce.lce_workspace_size(N, H, V, 0, False, lce.WS_FUSED_MIN)
+    assert fmin == fb - second and max(f, b) <= fmin <= f + b
+    assert lce.lce_workspace_size(N, H, V, 0, True, lce.WS_FUSED_MIN) == with_bias
+    assert lce.lce_workspace_size(N, H, V, 2048, False, lce.WS_FUSED_MIN) == \
+        lce.lce_workspace_size(N, H, V, 2048, False, lce.WS_FUSED)  # chunks too small to overlap
 
 
 @pytest.mark.parametrize("args,code", [
@@ -71,6 +80,12 @@ def test_workspace_size_rejects(args, code):
     with pytest.raises(lce.LCEError) as e:
         lce.lce_workspace_size(*args, False, lce.WS_FUSED)
     assert e.value.status == code
+
+
+def test_workspace_which_is_checked_4():
+    with pytest.raises(lce.LCEError) as e:
+        lce.lce_workspace_size(16, 64, 32, 0, False, 4)
+    assert e.value.status == 1
 
 
 def test_workspace_which_is_checked():

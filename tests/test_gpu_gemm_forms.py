@@ -4,7 +4,8 @@ CTAs on neighbouring SMs sharing 256x256 tiles (cta_group::2).  Each form is
 checked against float64 products (the bare GEMM core) and against the FP64
 oracle (the fused call), on shapes with ragged edges in every dimension,
 odd numbers of 128-row tiles (a pair whose second half lies past the
-rows), compacted chunks and split-K grad_X."""
+rows), compacted chunks, split-K grad_X, and chunks large enough for the
+forward to rescale the previous chunk's exponentials as a side job."""
 import numpy as np
 import pytest
 
@@ -61,6 +62,7 @@ def test_debug_gemm_forms(form, layout, M, N, K):
     (700, 192, 4100, True, 256),     # ragged rows and vocabulary, bias, 3 chunks
     (1300, 256, 2304, False, 640),   # ragged chunk of 20 rows
     (256, 512, 33000, False, 256),   # few output tiles: split-K grad_X
+    (9000, 128, 4096, False, 4096),  # chunks of >= 4096 rows: each forward rescales the previous chunk's E
 ])
 def test_fused_forms_match_oracle(form, N, H, V, bias, chunk):
     X, W, b, y = random_problem(31 + N, N, H, V, bias, ignore_frac=0.2)

@@ -250,3 +250,35 @@ def test_chunk_spanning_several_label_blocks():
         out = run_fused(X, W, b, y, chunk)
         assert out["status"] == 0
         check_against_oracle(out, ref, has_bias=True, acc_bound=bound)
+
+
+def test_overlapped_rescale_matches_oracle_and_recompute():
+    """Chunks of >= 4096 rows without a bias: each chunk's forward also turns
+    the previous chunk's kept exponentials into P (the epilogue warps' side
+    job), and chunk c-1's backward runs after chunk c's forward.  Every
+    output against the oracle, and grad_W_acc against the recomputing
+    lce_forward + lce_backward path."""
+    import torch
+    X, W, b, y = random_problem(91, 9000, 128, 4096, bias=False, ignore_frac=0.2)
+    ref = oracle_of(X, W, b, y)
+    bound = fp16_acc_bound(X, W, b, y, ref["lse"], 1.0 / max(ref["n_valid"], 1))
+    out = run_fused(X, W, b, y, 4096)
+    assert out["status"] == 0
+    check_against_oracle(out, ref, has_bias=False, acc_bound=bound)
+    Xd, Wd, yd = dev_bf16(X), dev_bf16(W), dev_i64(y)
+    f = lce.forward(Xd, Wd, None, yd, chunk_rows=4096)
+    g = lce.backward(Xd, Wd, None, yd, f["lse"], chunk_rows=4096)
+    assert lce.lce_check_status(g["ws"], torch.cuda.current_stream()) == 0
+    d = (out["grad_W_acc"].double() - g["grad_W_acc"].double()).abs().max().item()
+    assert d <= 2e-4 * g["grad_W_acc"].abs().max().item(), d  # both within 1e-4 of the oracle
+    # With only the minimum workspace the rescale runs as its own kernel,
+    # after the chunk's forward: the same arithmetic, so the same bits.
+    N, H = X.shape
+    V = W.shape[0]
+    nmin = lce.lce_workspace_size(N, H, V, 4096, False, lce.WS_FUSED_MIN)
+    assert nmin < lce.lce_workspace_size(N, H, V, 4096, False, lce.WS_FUSED)
+    seq = lce.fused(Xd, Wd, None, yd, chunk_rows=4096,
+                    ws=torch.empty(nmin, dtype=torch.uint8, device="cuda"))
+    assert lce.lce_check_status(seq["ws"], torch.cuda.current_stream()) == 0
+    for k in ("loss", "lse", "grad_X", "grad_W", "grad_W_acc"):
+        assert torch.equal(seq[k], out[k]), k
