@@ -136,9 +136,30 @@ def cpu_baseline(w, rows=256):
     y = L.labels(w)
     t, n = oracle_sample(w, rows, W_bits=W_bits, y=y)
     threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
-    return {"value": n / t, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"FP64 oracle forward+backward (numpy, float64 BLAS) on the first {n} of {w.N} rows "
-                      f"with all of W [{w.V}x{w.H}], {t:.1f} s"}
+    out = {"value": n / t, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+           "sample": f"FP64 oracle forward+backward (numpy, float64 BLAS) on the first {n} of {w.N} rows "
+                     f"with all of W [{w.V}x{w.H}], {t:.1f} s; tokens/s extrapolated from that sample",
+           "host_cores": os.cpu_count()}
+    one = cpu_baseline_one_thread(w, max(1, rows // 16))
+    if one is not None:
+        out["one_thread"] = one
+    return out
+
+
+def cpu_baseline_one_thread(w, rows):
+    """The same oracle on one host thread (BLAS limited to one thread), in a
+    fresh interpreter so the limit takes effect: {"value", "rows", "seconds"}."""
+    import subprocess
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import sys, json; sys.path.insert(0, %r); import bench, lce_inputs as L; "
+            "w = [x for x in L.WORKLOADS if x.name == %r][0]; t, n = bench.oracle_sample(w, %d); "
+            "print(json.dumps({'seconds': t, 'rows': n}))") % (ROOT, w.name, rows)
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
+    return {"value": d["rows"] / d["seconds"], "unit": "tokens/s", "rows": d["rows"], "seconds": d["seconds"]}
 
 
 def run_reference(args, w):
