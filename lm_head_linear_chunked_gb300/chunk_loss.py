@@ -19,8 +19,8 @@ from typing import Optional
 
 import torch
 
-from . import IGNORE_INDEX, WS_FORWARD, WS_FUSED, _flags, lce_check_status, lce_forward_ex, lce_fused_fwd_bwd_ex, \
-    lce_scale_grads, lce_workspace_size
+from . import IGNORE_INDEX, WS_FORWARD, WS_FUSED, WS_FUSED_MIN, _flags, lce_check_status, lce_forward_ex, \
+    lce_fused_fwd_bwd_ex, lce_scale_grads, lce_workspace_size
 
 
 def _flat_contiguous(t: torch.Tensor) -> torch.Tensor:
@@ -33,7 +33,7 @@ class ChunkedLinearCrossEntropy(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, hidden, weight, bias, labels, ignore_index: int, chunk_rows: int, check: bool,
-                grad_wanted: bool, reduction: str = "mean"):
+                grad_wanted: bool, reduction: str = "mean", overlap: bool = False):
         X = _flat_contiguous(hidden)
         y = labels.reshape(-1).to(torch.int64).contiguous()
         N, H = X.shape
@@ -52,7 +52,7 @@ class ChunkedLinearCrossEntropy(torch.autograd.Function):
             lce_forward_ex(N, H, V, X, weight, bias, y, ignore_index, chunk_rows, loss, lse, n_valid, ws, nws, stream,
                            flags)
         else:
-            nws = lce_workspace_size(N, H, V, chunk_rows, bias is not None, WS_FUSED)
+            nws = lce_workspace_size(N, H, V, chunk_rows, bias is not None, WS_FUSED if overlap else WS_FUSED_MIN)
             ws = torch.empty(nws, dtype=torch.uint8, device=dev)
             grad_X = torch.empty_like(X)
             grad_W_acc = torch.empty((V, H), dtype=torch.float32, device=dev)
@@ -83,13 +83,13 @@ class ChunkedLinearCrossEntropy(torch.autograd.Function):
                         grad_b_acc if grad_b is not None else None, grad_b,
                         torch.cuda.current_stream(grad_X.device))
         gx = grad_X.reshape(shape) if ctx.needs_input_grad[0] else None
-        return gx, grad_W, grad_b, None, None, None, None, None, None
+        return gx, grad_W, grad_b, None, None, None, None, None, None, None
 
 
 def linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor, labels: torch.Tensor,
                          bias: Optional[torch.Tensor] = None, ignore_index: int = IGNORE_INDEX,
                          chunk_rows: int = 0, check: bool = False, return_lse: bool = False,
-                         reduction: str = "mean"):
+                         reduction: str = "mean", overlap: bool = False):
     """Chunked linear cross-entropy with autograd.
 
     hidden [..., H] bf16, weight [V, H] bf16 (nn.Linear layout), labels [...]
@@ -97,14 +97,17 @@ def linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor, labels: tor
     mean (reduction="mean") or sum (reduction="sum") of the loss over valid
     positions (0 if none), and the per-row logsumexp if return_lse.
     chunk_rows = 0 lets the library choose.  check=True synchronises and
-    raises on a device-side error (bad label)."""
+    raises on a device-side error (bad label).  overlap=True gives the fused
+    call the larger workspace (one more chunk of fp16 exponentials) with
+    which each chunk's forward also rescales the previous chunk's softmax:
+    a little faster, the same results; the default keeps the minimum."""
     if chunk_rows < 0:
         raise ValueError("chunk_rows must not be negative")
     _flags(reduction, False)  # validates reduction
     grad_wanted = torch.is_grad_enabled() and any(
         t is not None and t.requires_grad for t in (hidden, weight, bias))
     loss, lse = ChunkedLinearCrossEntropy.apply(hidden, weight, bias, labels, ignore_index, chunk_rows, check,
-                                                grad_wanted, reduction)
+                                                grad_wanted, reduction, overlap)
     return (loss, lse) if return_lse else loss
 
 

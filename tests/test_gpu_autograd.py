@@ -64,3 +64,20 @@ def test_no_grad_forward_only():
     ref = oracle.forward(X, W, None, y)
     assert abs(float(loss.item()) - ref["loss"]) <= LOSS_RTOL * abs(ref["loss"])
     assert np.abs(host_f64(lse) - ref["lse"]).max() <= 1e-3
+
+
+def test_autograd_overlap_option_same_bits():
+    """overlap=True (the larger workspace: each chunk's forward rescales the
+    previous chunk's softmax) gives the same loss and gradients, bit for bit,
+    as the default minimum workspace."""
+    from lm_head_linear_chunked_gb300.chunk_loss import linear_cross_entropy
+    (X, W, b, y), (Xd, Wd, bd, yd), torch = _setup(33, 9000, 128, 2048, False)
+    grads = []
+    for overlap in (False, True):
+        Xd.grad = None
+        Wd.grad = None
+        loss = linear_cross_entropy(Xd, Wd, yd, chunk_rows=4096, check=True, overlap=overlap)
+        loss.backward()
+        grads.append((loss.detach().clone(), Xd.grad.clone(), Wd.grad.clone()))
+    for a, b_ in zip(*grads):
+        assert torch.equal(a, b_)
