@@ -20,8 +20,9 @@ constexpr int64_t AUTO_CHUNK_ROWS = 16384;
 // Smallest chunk whose forward hides the previous chunk's softmax rescale.
 constexpr int64_t OVERLAP_MIN_ROWS = 4096;
 // Tile-order groups: 4096 rows of X (32 MB at H = 4096) for the logits
-// passes, 2048 rows of P for grad_X; for the grad_W pass, as many 256-column tiles of the
-// fp16 X chunk as make about 32 MB (8 at 8192 rows, 4 at 16384).
+// passes, 2048 rows of P for grad_X (single form); for the grad_W pass, as
+// many 256-column tiles of the fp16 X chunk as make about 32 MB (4 at 16384
+// rows), or 64 MB in the pair form.
 constexpr int64_t LOGITS_GROUP_ROWS = 4096;
 constexpr int64_t GRADX_GROUP_ROWS = 2048;
 constexpr int64_t GROUP_BYTES = 32ll << 20;
@@ -467,7 +468,10 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             a.m_tiles = static_cast<int32_t>(mtf);
             a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
             a.k_blocks = static_cast<int32_t>(cdiv(pb.V, BK));
-            a.raster = 2;
+            // pair form: H tiles fastest, so that each wave covers whole rows of
+            // grad_X and every tile sharing a P row block runs at once (measured:
+            // grad_X 7% faster and ~20% fewer DRAM reads than 2048-row groups)
+            a.raster = form.pair ? 1 : 2;
             a.group_m = static_cast<int32_t>(GRADX_GROUP_ROWS / form.rows);
             a.M = rows;
             a.N = pb.H;
