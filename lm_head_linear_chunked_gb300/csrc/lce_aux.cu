@@ -63,11 +63,13 @@ __global__ void scale_kernel(WsHeader* hdr, float grad_scale, const float* d_gra
 }
 
 // lse_i = (M + log2 S) ln 2, where (M, S) merges the per-half-tile partial
-// (max, sum of 2^(t - max)).  One warp per row: lane k merges partials
-// k, k+32, ... in order (S <- S 2^(M - M') + s_t 2^(m_t - M') when a larger
-// max m_t = M' arrives, else S <- S + s_t 2^(m_t - M)); the 32 results are
-// then merged by a butterfly in a fixed order, so lse does not depend on the
-// chunk size.  Row loss = lse_i - z[i, y_i] for valid rows, else 0.
+// (max, sum of 2^(t - max)) pairs of row i.  Each row's partial list is cut
+// into 4 contiguous parts, merged in order by 4 threads (S <- S 2^(M - M') +
+// s_t 2^(m_t - M') when a larger max m_t = M' arrives, else S <- S +
+// s_t 2^(m_t - M)); parts 0+1 and 2+3, then the two halves, are merged in
+// that fixed order, so lse does not depend on the chunk size.  A warp holds
+// 8 rows: the 8 lanes of a part read 8 consecutive rows of a partial, one
+// 32-byte sector.  Row loss = lse_i - z[i, y_i] for valid rows, else 0.
 __device__ __forceinline__ void merge_partial(float& M, float& S, float m, float s) {
     if (m > M) {
         S = S * exp2f(M - m) + s;
@@ -83,13 +85,28 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       int64_t ignore_index, float* __restrict__ lse,
                                                       float* __restrict__ row_loss) {
     const int lane = threadIdx.x & 31;
-    const int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
+    const int part = lane >> 3;
+    const int64_t r = (blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5)) * 8 + (lane & 7);
     const bool ok = r < rows;
+    const int64_t per = (n_pt + 3) / 4;
+    const int64_t t0 = part * per, t1 = t0 + per < n_pt ? t0 + per : n_pt;
     float M = -INFINITY, S = 0.f;
-    if (ok)
-        for (int64_t t = lane; t < n_pt; t += 32) merge_partial(M, S, pm[t * ldp + r], ps[t * ldp + r]);
+    if (ok) {
+        int64_t t = t0;
+        for (; t + 4 <= t1; t += 4) {
+            float m4[4], s4[4];
 #pragma unroll
-    for (int o = 1; o <= 16; o <<= 1) {
+            for (int k = 0; k < 4; ++k) {
+                m4[k] = pm[(t + k) * ldp + r];
+                s4[k] = ps[(t + k) * ldp + r];
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) merge_partial(M, S, m4[k], s4[k]);
+        }
+        for (; t < t1; ++t) merge_partial(M, S, pm[t * ldp + r], ps[t * ldp + r]);
+    }
+#pragma unroll
+    for (int o = 8; o <= 16; o <<= 1) {
         const float M2 = __shfl_xor_sync(0xFFFFFFFFu, M, o);
         const float S2 = __shfl_xor_sync(0xFFFFFFFFu, S, o);
         const bool lower = (lane & o) == 0;  // both partners merge (lower, upper)
@@ -98,20 +115,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         M = Ma;
         S = Sa;
     }
-    if (!ok || lane != 0) return;
+    if (!ok || part != 0) return;
     const float l = (M + log2f(S)) * LN2_F;
     lse[r] = l;
     if (row_loss) row_loss[r] = (y[r] != ignore_index) ? l - zt[r] : 0.f;
 }
 
-// The fused path's softmax without recomputing the logits: the forward
-// stored E = fp16(2^(t - m) 2^15) per (valid row, 128-column half of a vocab
-// tile), with m that half tile's max, at the row's compacted position; here, once lse is
-// known, P = fp16(E 2^(m - lse log2 e)) in place (= fp16(p 2^15)).  Compact
-// rows from n_valid up to the next multiple of 64 are zeroed (the K tail of
-// the grad_W product).  One block covers 32 compact rows of one vocab tile:
-// 32 threads x 8 columns, 8 rows at a time.  With gb_part it also writes the
-// block's fp32 column sums of p (fixed row order).
 __global__ void __launch_bounds__(256) p_rescale_kernel(uint16_t* __restrict__ P, int64_t ldg, int64_t rows,
                                                         int64_t V, const float* __restrict__ pm, int64_t ldp,
                                                         const float* __restrict__ lse,
@@ -669,8 +678,8 @@ cudaError_t launch_scale(WsHeader* hdr, float grad_scale, const float* d_grad_ou
 cudaError_t launch_combine(const float* part_m, const float* part_s, int64_t n_pt, int64_t ldp, int64_t rows,
                            const float* zt, const int64_t* y, int64_t ignore_index, float* lse, float* row_loss,
                            cudaStream_t s) {
-    const int threads = 256;  // 8 rows per block, one warp per row
-    const int64_t blocks = (rows + 7) / 8;
+    const int threads = 256;  // 8 warps of 8 rows each
+    const int64_t blocks = (rows + 63) / 64;
     combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(part_m, part_s, n_pt, ldp, rows, zt, y,
                                                                       ignore_index, lse, row_loss);
     return cudaGetLastError();
