@@ -383,9 +383,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     auto forward_chunk = [&](int64_t c, uint16_t* Gc, float* pmc, int64_t side) -> lce_status_t {
         const int64_t r0 = c * p.C;
         const int64_t rows = (pb.N - r0) < p.C ? (pb.N - r0) : p.C;
-        const int64_t mt = cdiv(rows, BM);        // 128-row tiles (grad_b partial rows)
         const int64_t mtf = cdiv(rows, form.rows);  // tiles of the GEMM form
-        (void)mt;
         GemmArgs a = base_args(hdr);
         a.m_tiles = static_cast<int32_t>(mtf);
         a.n_tiles = static_cast<int32_t>(p.n_vt);
