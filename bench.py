@@ -53,12 +53,13 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # they were captured with: DRAM_BYTES_SOURCES lists the files that decide a
 # GEMM launch's traffic and DRAM_BYTES_DIGEST their SHA-256 at capture time.
 # When the digest no longer matches, roofline.traffic is reported as null.
-DRAM_BYTES_PER_LAUNCH = {"grad_w": 24.38e9 + 2.48e9, "grad_x": 35.56e9 + 0.12e9,
-                         "logits_lse": 13.94e9 + 9.63e9, "recomputed_logits_softmax": None}
+DRAM_BYTES_PER_LAUNCH = {"grad_w": 27.72e9 + 2.48e9, "grad_x": 41.17e9 + 0.12e9,
+                         "logits_lse": 16.96e9 + 9.63e9, "recomputed_logits_softmax": None}
 DRAM_BYTES_CHUNK_ROWS = 16384  # the chunk size those launches ran with
-DRAM_BYTES_SOURCES = ["csrc/lce_gemm.cuh", "csrc/lce_internal.cuh", "csrc/lce_ptx.cuh", "csrc/lce_api.cu",
-                      "csrc/lce_gemm_logits.cu", "csrc/lce_gemm_grads.cu"]
-DRAM_BYTES_DIGEST = "e8f6ef56433392e0"
+DRAM_BYTES_FORM = "pair"  # and their GEMM form
+DRAM_BYTES_SOURCES = ["csrc/lce_gemm.cuh", "csrc/lce_gemm_pair.cuh", "csrc/lce_internal.cuh", "csrc/lce_ptx.cuh",
+                      "csrc/lce_api.cu", "csrc/lce_gemm_logits.cu", "csrc/lce_gemm_grads.cu"]
+DRAM_BYTES_DIGEST = "1d33c122c9d34416"
 
 
 def gemm_source_digest() -> str:
@@ -531,10 +532,11 @@ def run_ours(args, w):
         "roofline": {"bound": "tensor", "achieved": dom_tflops, "peak": sustained, "unit": "TFLOP/s",
                      "frac": dom_tflops / sustained,
                      "traffic": DRAM_BYTES_PER_LAUNCH.get(dom) if args.workload == WORKLOAD and not args.shape
-                     and C == DRAM_BYTES_CHUNK_ROWS and gemm_source_digest() == DRAM_BYTES_DIGEST else None,
+                     and C == DRAM_BYTES_CHUNK_ROWS and gemm_form == DRAM_BYTES_FORM
+                     and gemm_source_digest() == DRAM_BYTES_DIGEST else None,
                      "traffic_source": f"ncu capture of sources {DRAM_BYTES_DIGEST}; these sources "
                                        f"{gemm_source_digest()}",
-                     "kernel": f"gemm_kernel ({dom})" + (
+                     "kernel": f"{'gemm_pair_kernel' if gemm_form == 'pair' else 'gemm_kernel'} ({dom})" + (
                          ", which also turns the previous chunk's kept exponentials into the softmax (4*C*V bytes) "
                          "with its epilogue warps" if dom == "logits_lse" and overlapped else ""),
                      "roles": {k: {"tflops": 2.0 * N * H * V / n_chunks / (prof[k][0] / prof[k][1] / 1e3) / 1e12,
