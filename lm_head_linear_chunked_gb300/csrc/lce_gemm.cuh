@@ -308,7 +308,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         // and with a.g set, E = fp16(2^(t - max) * 2^P_SCALE_EXP) for the
         // backward (rescaled to P once lse is known).
         const int64_t yr = row_ok ? a.y[row] : a.ignore_index;
-        float mx = -INFINITY, zt = 0.f;
+        // The max is taken over z and scaled once: rounding is monotone, so
+        // max(z) * log2(e) rounds to the same float as max(z * log2(e)).
+        float mz = -INFINITY, zt = 0.f;
         bool got = false;
 #pragma unroll 1
         for (int j = j0; j < j0 + BN / 64; ++j) {
@@ -321,12 +323,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
             const int64_t d = yr - c0;
             const int kk = (d >= 0 && d < 32) ? static_cast<int>(d) : -1;
             got |= kk >= 0;
+            if (__any_sync(0xFFFFFFFFu, kk >= 0)) {  // a label of the warp's rows lies in these columns
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                zt = (i == kk) ? v[i] : zt;
-                if (i < nv) mx = fmaxf(mx, v[i] * LOG2E_F);
+                for (int i = 0; i < 32; ++i) zt = (i == kk) ? v[i] : zt;
+            }
+            if (nv == 32) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mz = fmaxf(mz, v[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (i < nv) mz = fmaxf(mz, v[i]);
             }
         }
+        const float mx = mz * LOG2E_F;
         float sm = 0.f;
 #pragma unroll 1
         for (int j = j0; j < j0 + BN / 64; ++j) {
@@ -336,11 +346,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
             tmem_load_32cols(taddr + 32 * j, v);
             const int nv = static_cast<int>(min64(32, a.N - c0));
             if (a.bias) add_bias32(v, a.bias + c0, nv);
+            if (nv == 32) {  // a whole chunk (all but the vocabulary's last): no per-column checks
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float e = (i < nv) ? fast_exp2(v[i] * LOG2E_F - mx) : 0.f;
-                sm += e;
-                v[i] = e * P_SCALE;
+                for (int i = 0; i < 32; ++i) {
+                    const float e = fast_exp2(v[i] * LOG2E_F - mx);
+                    sm += e;
+                    v[i] = e * P_SCALE;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float e = (i < nv) ? fast_exp2(v[i] * LOG2E_F - mx) : 0.f;
+                    sm += e;
+                    v[i] = e * P_SCALE;
+                }
             }
             if (a.g && prow >= 0) store_f16_32(a.g + prow * a.ldg + c0, v, static_cast<int>(min64(32, a.ldg - c0)));
         }
