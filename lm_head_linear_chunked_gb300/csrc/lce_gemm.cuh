@@ -238,19 +238,27 @@ __device__ __forceinline__ void side_init(const GemmArgs& a, SideJob& j, int64_t
 __device__ __forceinline__ void side_unit(const GemmArgs& a, const SideJob& j, int64_t u, int lane) {
     const int64_t tile = u % a.n_tiles, rb = u / a.n_tiles;
     const int64_t c = tile * 256 + lane * 8;
-    if (c >= a.ldg) return;
-    const float* pm = a.side_pm + (2 * tile + (lane >> 4)) * a.ldp;  // one max per 128-column half tile
+    // The unit's 16 factors (8 rows x 2 half tiles, one max per 128-column
+    // half tile) are computed once, by lane 8h + i for row i of half h, and
+    // handed to the lanes of that half by shuffles.
+    float fl = 0.f;
+    {
+        const int64_t r8 = rb * 8 + (lane & 7);
+        if (lane < 16 && r8 < j.nv) {
+            const int64_t r = a.side_crow[r8];  // chunk row
+            const float* pm = a.side_pm + (2 * tile + (lane >> 3)) * a.ldp;
+            fl = exp2f(pm[r] - a.side_lse[r] * LOG2E_F);
+        }
+    }
     float f[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = __shfl_sync(0xFFFFFFFFu, fl, (lane >> 4) * 8 + i);
+    if (c >= a.ldg) return;
     uint4 w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int64_t r8 = rb * 8 + i;
-        f[i] = 0.f;
-        if (r8 < j.nv) {
-            const int64_t r = a.side_crow[r8];  // chunk row
-            f[i] = exp2f(pm[r] - a.side_lse[r] * LOG2E_F);
-            w[i] = *reinterpret_cast<const uint4*>(a.side_p + r8 * a.ldg + c);
-        }
+        if (r8 < j.nv) w[i] = *reinterpret_cast<const uint4*>(a.side_p + r8 * a.ldg + c);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
