@@ -64,12 +64,15 @@ __global__ void scale_kernel(WsHeader* hdr, float grad_scale, const float* d_gra
 
 // lse_i = (M + log2 S) ln 2, where (M, S) merges the per-half-tile partial
 // (max, sum of 2^(t - max)) pairs of row i.  Each row's partial list is cut
-// into 4 contiguous parts, merged in order by 4 threads (S <- S 2^(M - M') +
-// s_t 2^(m_t - M') when a larger max m_t = M' arrives, else S <- S +
-// s_t 2^(m_t - M)); parts 0+1 and 2+3, then the two halves, are merged in
-// that fixed order, so lse does not depend on the chunk size.  A warp holds
-// 8 rows: the 8 lanes of a part read 8 consecutive rows of a partial, one
-// 32-byte sector.  Row loss = lse_i - z[i, y_i] for valid rows, else 0.
+// into 32 contiguous parts, each merged in order by one thread (S <- S
+// 2^(M - M') + s_t 2^(m_t - M') when a larger max m_t = M' arrives, else
+// S <- S + s_t 2^(m_t - M)).  The 32 part results are merged by a fixed
+// tree: within a warp, parts 4w .. 4w+3 as (0+1) + (2+3) by shuffles; then
+// the block's 8 warp results pairwise, ((0+1) + (2+3)) + ((4+5) + (6+7)),
+// through shared memory.  The tree depends only on the partial count, so lse
+// does not depend on the chunk size.  A block holds 8 rows: the 8 lanes of a
+// part read 8 consecutive rows of a partial, one 32-byte sector.  Row loss =
+// lse_i - z[i, y_i] for valid rows, else 0.
 __device__ __forceinline__ void merge_partial(float& M, float& S, float m, float s) {
     if (m > M) {
         S = S * exp2f(M - m) + s;
@@ -84,24 +87,25 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const float* __restrict__ zt, const int64_t* __restrict__ y,
                                                       int64_t ignore_index, float* __restrict__ lse,
                                                       float* __restrict__ row_loss) {
-    const int lane = threadIdx.x & 31;
-    const int part = lane >> 3;
-    const int64_t r = (blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5)) * 8 + (lane & 7);
+    __shared__ float wm[8][8], wsum[8][8];  // [warp][row of the block]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int part = warp * 4 + (lane >> 3);
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (lane & 7);
     const bool ok = r < rows;
-    const int64_t per = (n_pt + 3) / 4;
-    const int64_t t0 = part * per, t1 = t0 + per < n_pt ? t0 + per : n_pt;
+    const int64_t per = (n_pt + 31) / 32;
+    const int64_t t0 = part * per < n_pt ? part * per : n_pt, t1 = t0 + per < n_pt ? t0 + per : n_pt;
     float M = -INFINITY, S = 0.f;
     if (ok) {
         int64_t t = t0;
-        for (; t + 4 <= t1; t += 4) {
-            float m4[4], s4[4];
+        for (; t + 8 <= t1; t += 8) {
+            float m8[8], s8[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                m4[k] = pm[(t + k) * ldp + r];
-                s4[k] = ps[(t + k) * ldp + r];
+            for (int k = 0; k < 8; ++k) {
+                m8[k] = pm[(t + k) * ldp + r];
+                s8[k] = ps[(t + k) * ldp + r];
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) merge_partial(M, S, m4[k], s4[k]);
+            for (int k = 0; k < 8; ++k) merge_partial(M, S, m8[k], s8[k]);
         }
         for (; t < t1; ++t) merge_partial(M, S, pm[t * ldp + r], ps[t * ldp + r]);
     }
@@ -115,8 +119,23 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         M = Ma;
         S = Sa;
     }
-    if (!ok || part != 0) return;
-    const float l = (M + log2f(S)) * LN2_F;
+    if (lane < 8) {
+        wm[warp][lane] = M;
+        wsum[warp][lane] = S;
+    }
+    __syncthreads();
+    if (warp != 0 || lane >= 8 || !ok) return;
+    float m[8], sv[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        m[w] = wm[w][lane];
+        sv[w] = wsum[w][lane];
+    }
+#pragma unroll
+    for (int step = 1; step < 8; step <<= 1)
+#pragma unroll
+        for (int w = 0; w < 8; w += 2 * step) merge_partial(m[w], sv[w], m[w + step], sv[w + step]);
+    const float l = (m[0] + log2f(sv[0])) * LN2_F;
     lse[r] = l;
     if (row_loss) row_loss[r] = (y[r] != ignore_index) ? l - zt[r] : 0.f;
 }
@@ -678,8 +697,8 @@ cudaError_t launch_scale(WsHeader* hdr, float grad_scale, const float* d_grad_ou
 cudaError_t launch_combine(const float* part_m, const float* part_s, int64_t n_pt, int64_t ldp, int64_t rows,
                            const float* zt, const int64_t* y, int64_t ignore_index, float* lse, float* row_loss,
                            cudaStream_t s) {
-    const int threads = 256;  // 8 warps of 8 rows each
-    const int64_t blocks = (rows + 63) / 64;
+    const int threads = 256;  // 8 rows, 32 threads each
+    const int64_t blocks = (rows + 7) / 8;
     combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(part_m, part_s, n_pt, ldp, rows, zt, y,
                                                                       ignore_index, lse, row_loss);
     return cudaGetLastError();
