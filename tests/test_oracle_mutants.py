@@ -34,6 +34,11 @@ MUTANTS = {
     "sum_loss_divided": ("        loss = total\n", "        loss = total / max(n_valid, 1)\n"),
     "sum_scale_divided": ("        return float(grad_scale) * float(grad_output)\n",
                           "        return float(grad_scale) * float(grad_output) / max(n_valid, 1)\n"),
+    "lse_missing_max": ("    return m + np.log(np.exp(z - m[:, None]).sum(axis=1))\n",
+                        "    return np.log(np.exp(z - m[:, None]).sum(axis=1))\n"),
+    "softmax_not_normalised": ("    G = np.exp(z - lse[:, None])\n", "    G = np.exp(z - z.max(axis=1)[:, None])\n"),
+    "ignored_rows_in_loss": ("    total = float((lse[ok] - zt[ok]).sum())\n", "    total = float((lse - zt).sum())\n"),
+    "loss_sign": ("    total = float((lse[ok] - zt[ok]).sum())\n", "    total = float((zt[ok] - lse[ok]).sum())\n"),
     "target_logit_wrong_column": ("        zt[r0:r1][ok] = z[np.nonzero(ok)[0], yy[ok]]\n",
                                   "        zt[r0:r1][ok] = z[np.nonzero(ok)[0], 0]\n"),
 }
