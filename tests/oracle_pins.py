@@ -367,7 +367,22 @@ def pin_row_sampled_pieces(orc):
     return fails
 
 
-ALL_PINS = [pin_zero_weight_closed_form, pin_rows_sum_to_zero, pin_ignored_rows,
+def pin_bf16_decode(orc):
+    """bf16 bit patterns decode to the values their IEEE fields define:
+    sign, 8 exponent bits (bias 127), 7 fraction bits; subnormals 0.f 2^-126.
+    Written as hand-derived constants, independent of any decoder."""
+    cases = {0x3F80: 1.0, 0xC020: -2.5, 0x0001: 2.0 ** -133, 0x7F7F: (2 - 2.0 ** -7) * 2.0 ** 127,
+             0x4049: 3.140625, 0x0080: 2.0 ** -126, 0xBE00: -0.125, 0x4300: 128.0}
+    bits = np.array(list(cases), dtype=np.uint16)
+    got = orc.as_f64(bits)
+    fails = [f"bf16 decode {hex(b)} -> {g} != {cases[b]}" for b, g in zip(cases, got) if g != cases[b]]
+    z = orc.as_f64(np.array([0x8000], dtype=np.uint16))[0]
+    if not (z == 0.0 and np.signbit(z)):
+        fails.append("bf16 decode 0x8000 is not -0.0")
+    return fails
+
+
+ALL_PINS = [pin_bf16_decode, pin_zero_weight_closed_form, pin_rows_sum_to_zero, pin_ignored_rows,
             pin_finite_differences, pin_shift_invariance, pin_row_permutation,
             pin_torch_cross_entropy, pin_torch_cross_entropy_sum, pin_finite_differences_sum,
             pin_single_class, pin_no_valid_rows,

@@ -39,6 +39,12 @@ MUTANTS = {
     "softmax_not_normalised": ("    G = np.exp(z - lse[:, None])\n", "    G = np.exp(z - z.max(axis=1)[:, None])\n"),
     "ignored_rows_in_loss": ("    total = float((lse[ok] - zt[ok]).sum())\n", "    total = float((lse - zt).sum())\n"),
     "loss_sign": ("    total = float((lse[ok] - zt[ok]).sum())\n", "    total = float((zt[ok] - lse[ok]).sum())\n"),
+    "bf16_decode_shift_15": ("        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)\n",
+                             "        return (a.astype(np.uint32) << 15).view(np.float32).astype(np.float64)\n"),
+    "bf16_decode_as_float16": ("        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)\n",
+                               "        return a.view(np.float16).astype(np.float64)\n"),
+    "bf16_decode_drops_sign": ("        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)\n",
+                               "        return ((a.astype(np.uint32) & 0x7FFF) << 16).view(np.float32).astype(np.float64)\n"),
     "target_logit_wrong_column": ("        zt[r0:r1][ok] = z[np.nonzero(ok)[0], yy[ok]]\n",
                                   "        zt[r0:r1][ok] = z[np.nonzero(ok)[0], 0]\n"),
 }
