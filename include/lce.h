@@ -45,8 +45,8 @@
  *    short workspace) are returned before anything is enqueued.  Errors
  *    found on the device (a label outside [0,V) that is not ignore_index,
  *    a pipeline wait that timed out) are recorded in a status word inside
- *    `ws` and read back by lce_check_status(); outputs are then undefined.
- *    No kernel traps.
+ *    `ws` and read back by lce_check_status(); the loss is then NaN and the
+ *    other outputs are undefined.  No kernel traps.
  *  - n_valid == 0 gives loss = 0 and all-zero gradients (the trainer's
  *    guard against dividing by zero); lse is still written for every row,
  *    ignored rows included.
@@ -201,7 +201,8 @@ LCE_API lce_status_t lce_scale_grads(int64_t N, int64_t H, int64_t V, const floa
 
 /* Synchronises `stream`, then returns the device status of the last call
  * that used workspace `ws` (LCE_OK, LCE_ERR_LABEL_RANGE, LCE_ERR_TIMEOUT),
- * or LCE_ERR_CUDA if the stream reported an error. */
+ * or LCE_ERR_CUDA if the stream reported an error.  A call that found an
+ * error on the device also writes NaN to its loss. */
 LCE_API lce_status_t lce_check_status(const void* ws, lce_stream_t stream);
 
 /* Static, human-readable name of a status code. */
@@ -249,15 +250,22 @@ LCE_API lce_status_t lce_debug_wait_timeout(uint32_t limit_us, void* ws, size_t 
  * any stream capture.  Every call on a device uses the same array and
  * leaves its contents behind: calls whose work may overlap on the GPU
  * (different streams, or different host threads) race on it, so issue
- * them in one stream order.  lce_check_status() is not available for this
- * entry point's device status; errors it finds on the device are not
- * reported. */
+ * them in one stream order.  Errors found on the device (a label outside
+ * [0, V) that is not ignore_index, a timed-out wait) make the loss NaN;
+ * lce_static_ws_check_status() reads their status. */
 #define LCE_STATIC_SCRATCH_BYTES (32u << 20)
 LCE_API lce_status_t lce_forward_static_ws(int64_t N, int64_t H, int64_t V,
                                    const lce_bf16* X, const lce_bf16* W, const lce_bf16* b,
                                    const int64_t* y, int64_t ignore_index, int64_t chunk_rows,
                                    float* loss, float* lse, int64_t* n_valid,
                                    lce_stream_t stream);
+
+/* The device status of the last lce_forward_static_ws call on the current
+ * device, like lce_check_status() for a caller's workspace: synchronises
+ * `stream` (the stream of that call), then returns LCE_OK,
+ * LCE_ERR_LABEL_RANGE or LCE_ERR_TIMEOUT, or LCE_ERR_CUDA if the stream
+ * reported an error.  Allocates nothing. */
+LCE_API lce_status_t lce_static_ws_check_status(lce_stream_t stream);
 
 /* lce_set_gemm_form: the tensor-core GEMM form of the calls this process
  * makes after it (each call reads the setting once, when it is made).

@@ -24,6 +24,7 @@ __all__ = [
     "lce_workspace_size", "lce_chunk_rows", "lce_forward", "lce_backward", "lce_fused_fwd_bwd",
     "lce_check_status", "lce_status_string", "lce_debug_gemm", "lce_debug_wait_timeout",
     "lce_profile_begin", "lce_profile_end", "PROFILE_KINDS", "lce_forward_static_ws", "STATIC_SCRATCH_BYTES",
+    "lce_static_ws_check_status",
     "lce_scale_grads",
     "workspace", "forward", "backward", "fused",
 ]
@@ -63,6 +64,7 @@ _SIGS = {
     "lce_debug_gemm": [ctypes.c_int, _I64, _I64, _I64, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "lce_debug_wait_timeout": [ctypes.c_uint32, _P, ctypes.c_size_t, _P],
     "lce_forward_static_ws": [_I64, _I64, _I64, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _P],
+    "lce_static_ws_check_status": [_P],
     "lce_scale_grads": [_I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P],
     "lce_set_gemm_form": [ctypes.c_int],
     "lce_gemm_pair_slots": [],
@@ -207,6 +209,12 @@ def lce_forward_static_ws(N, H, V, X, W, b, y, ignore_index, chunk_rows, loss, l
     _check(lib().lce_forward_static_ws(N, H, V, _ptr(X), _ptr(W), _ptr(b), _ptr(y), ignore_index, chunk_rows,
                                        _ptr(loss), _ptr(lse), _ptr(n_valid), _stream(stream)),
            "lce_forward_static_ws")
+
+
+def lce_static_ws_check_status(stream) -> int:
+    """Synchronises the stream; returns the device status code of the last
+    lce_forward_static_ws call on the current device (no raise)."""
+    return lib().lce_static_ws_check_status(_stream(stream))
 
 
 def lce_scale_grads(N, H, V, d_grad_output, grad_X, grad_W_acc, grad_W, grad_b_acc, grad_b, stream) -> None:

@@ -58,8 +58,8 @@ struct Plan {
     // fused call: chunk c's forward rescales chunk c-1's E (two E and two
     // half-tile-max buffers)
     bool overlap;
-    size_t off_row_loss, off_zt, off_pm, off_ps, off_g, off_gb, off_keys, off_runs, off_nrun, off_counts, off_w16,
-        off_x16, off_dmap, off_crow, off_nvc, off_split, off_g2, off_pm2, total;
+    size_t off_row_loss, off_zt, off_pm, off_ps, off_g, off_gb, off_keys, off_runs, off_nrun, off_lcsum, off_w16,
+        off_x16, off_dmap, off_crow, off_nvc, off_split, off_g2, off_pm2, off_tcoef, total;
 };
 
 lce_status_t check_sizes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows) {
@@ -104,13 +104,14 @@ lce_status_t make_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, bool
     p->off_row_loss = take(fwd, static_cast<size_t>(N) * 4);
     p->off_zt = take(fwd, static_cast<size_t>(p->C) * 4);
     p->off_pm = take(fwd, static_cast<size_t>(2 * p->n_vt) * p->C * 4);  // one per 128-column half tile
-    p->off_ps = take(fwd, static_cast<size_t>(2 * p->n_vt) * p->C * 4);
+    // the forward's half-tile sums, or the recompute's half-tile sums of P
+    p->off_ps = take(true, static_cast<size_t>(2 * p->n_vt) * p->C * 4);
     p->off_g = take(bwd, static_cast<size_t>(p->C) * p->ldg * 2);
     p->off_gb = take(bwd && has_bias, static_cast<size_t>(p->mt_chunk) * 4 * V * 4);
     p->off_keys = take(bwd, static_cast<size_t>(p->n_chunks) * p->label_blocks_per_chunk * LABEL_BLOCK * 8);
     p->off_runs = take(bwd, static_cast<size_t>(p->n_chunks) * p->label_blocks_per_chunk * LABEL_BLOCK * 8);
     p->off_nrun = take(bwd, static_cast<size_t>(p->n_chunks) * p->label_blocks_per_chunk * 4);
-    p->off_counts = take(bwd && has_bias, static_cast<size_t>(V) * 4);
+    p->off_lcsum = take(bwd && has_bias, static_cast<size_t>(V) * 4);
     p->off_w16 = take(bwd, static_cast<size_t>(V) * H * 2);
     p->off_x16 = take(bwd, static_cast<size_t>(p->C) * H * 2);
     p->off_dmap = take(bwd, static_cast<size_t>(N) * 4);
@@ -119,6 +120,7 @@ lce_status_t make_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, bool
     p->off_split = take(bwd && p->gradx_splits > 1, static_cast<size_t>(p->gradx_splits) * p->C * H * 4);
     p->off_g2 = take(p->overlap, static_cast<size_t>(p->C) * p->ldg * 2);
     p->off_pm2 = take(p->overlap, static_cast<size_t>(2 * p->n_vt) * p->C * 4);
+    p->off_tcoef = take(bwd, static_cast<size_t>(N) * 4);  // c_i = p_{i,y_i} - 1 of every row
     p->total = off;
     return LCE_OK;
 }
@@ -336,7 +338,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     float* row_loss = do_fwd ? reinterpret_cast<float*>(wsb + p.off_row_loss) : nullptr;
     float* zt = do_fwd ? reinterpret_cast<float*>(wsb + p.off_zt) : nullptr;
     float* pm = do_fwd ? reinterpret_cast<float*>(wsb + p.off_pm) : nullptr;
-    float* ps = do_fwd ? reinterpret_cast<float*>(wsb + p.off_ps) : nullptr;
+    float* ps = reinterpret_cast<float*>(wsb + p.off_ps);
     uint16_t* G = do_bwd ? reinterpret_cast<uint16_t*>(wsb + p.off_g) : nullptr;
     float* gb = (do_bwd && pb.b) ? reinterpret_cast<float*>(wsb + p.off_gb) : nullptr;
     unsigned long long* keys = do_bwd ? reinterpret_cast<unsigned long long*>(wsb + p.off_keys) : nullptr;
@@ -348,7 +350,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     int* crow = do_bwd ? reinterpret_cast<int*>(wsb + p.off_crow) : nullptr;  // compacted row -> chunk row
     int* nvc = do_bwd ? reinterpret_cast<int*>(wsb + p.off_nvc) : nullptr;    // valid rows per chunk
     float* split_out = (do_bwd && p.gradx_splits > 1) ? reinterpret_cast<float*>(wsb + p.off_split) : nullptr;
-    int* counts = (do_bwd && pb.b) ? reinterpret_cast<int*>(wsb + p.off_counts) : nullptr;
+    float* lcsum = (do_bwd && pb.b) ? reinterpret_cast<float*>(wsb + p.off_lcsum) : nullptr;  // sum of c per label
+    float* tcoef = do_bwd ? reinterpret_cast<float*>(wsb + p.off_tcoef) : nullptr;
     uint16_t* G2 = p.overlap ? reinterpret_cast<uint16_t*>(wsb + p.off_g2) : nullptr;
     float* pm2 = p.overlap ? reinterpret_cast<float*>(wsb + p.off_pm2) : nullptr;
 
@@ -361,8 +364,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     if (do_bwd && !map_f32_acc(&mAcc, o.grad_W_acc, pb.V, pb.H, pb.H)) return LCE_ERR_CUDA;
 
     LCE_TRY_CUDA(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s));
-    if (counts) LCE_TRY_CUDA(cudaMemsetAsync(counts, 0, static_cast<size_t>(pb.V) * 4, s));
-    LCE_LAUNCH(PK_OTHER, launch_prepass(pb.y, pb.N, pb.V, pb.ignore_index, hdr, counts, s));
+    if (lcsum) LCE_TRY_CUDA(cudaMemsetAsync(lcsum, 0, static_cast<size_t>(pb.V) * 4, s));
+    LCE_LAUNCH(PK_OTHER, launch_prepass(pb.y, pb.N, pb.V, pb.ignore_index, hdr, nullptr, s));
     if (do_bwd) {
         LCE_LAUNCH(PK_OTHER, launch_scale(hdr, o.grad_scale, o.d_grad_output, nullptr, sum_reduction, s));
         LCE_LAUNCH(PK_OTHER, launch_label_sort(pb.y, pb.N, p.C, p.label_blocks_per_chunk,
@@ -415,8 +418,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             a.side_rows = (pb.N - sr0) < p.C ? (pb.N - sr0) : p.C;
         }
         LCE_LAUNCH(PK_LSE, launch_gemm(MODE_LSE, mX_k, mW_k, mW_k, a, grid_of(form, mtf * p.n_vt), s, form.pair));
-        LCE_LAUNCH(PK_OTHER, launch_combine(pmc, ps, 2 * p.n_vt, p.C, rows, zt, pb.y + r0, pb.ignore_index,
-                                            o.lse + r0, row_loss + r0, s));
+        LCE_LAUNCH(PK_OTHER, launch_combine(pmc, ps, 2 * p.n_vt, p.C, rows, zt, pb.y + r0, pb.ignore_index, pb.V,
+                                            o.lse + r0, row_loss + r0, tcoef ? tcoef + r0 : nullptr, s));
         return LCE_OK;
     };
     // The backward of chunk c; `rescaled`: its E was already turned into P.
@@ -449,10 +452,13 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             a.ldg = p.ldg;
             a.gb_part = gb;
             a.row_map = dmap + r0;
+            a.part_s = ps;
+            a.ldp = p.C;
             LCE_LAUNCH(PK_P, launch_gemm(MODE_G, mX_k, mW_k, mW_k, a, grid_of(form, mtf * p.n_vt), s, form.pair));
+            // c_i = -(sum of the row's non-target P), in a fixed order
+            LCE_LAUNCH(PK_OTHER, launch_combine(nullptr, ps, 2 * p.n_vt, p.C, rows, nullptr, pb.y + r0,
+                                                pb.ignore_index, pb.V, nullptr, nullptr, tcoef + r0, s));
         }
-        if (gb)
-            LCE_LAUNCH(PK_OTHER, launch_grad_b(gb, mt * 4, pb.V, hdr, counts, o.grad_b_acc, o.grad_b, first, last, s));
         // P and X_c maps bounded to this chunk's rows: rows past it read as zero
         LCE_LAUNCH(PK_OTHER, launch_gather_f16(pb.X + r0 * pb.H, pb.H, crow + r0, nvc + c, rows, &hdr->amax_x_bits,
                                                X16, do_fwd ? nullptr : Gc, p.ldg, s));
@@ -483,6 +489,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             a.V = pb.V;
             a.b_amax_bits = &hdr->amax_w_bits;
             a.row_map = crow + r0;
+            a.tcoef = tcoef + r0;
             a.dyn_rows = nvc + c;
             a.k_splits = static_cast<int32_t>(p.gradx_splits);
             a.k_per_split = static_cast<int32_t>(cdiv(a.k_blocks, p.gradx_splits));
@@ -495,7 +502,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             if (split_out)
                 LCE_LAUNCH(PK_GRADX, launch_gradx_split_reduce(split_out, p.gradx_splits, p.C * pb.H, pb.H, crow + r0,
                                                                nvc + c, rows, pb.y + r0, pb.ignore_index, pb.V,
-                                                               pb.W, hdr, o.grad_X + r0 * pb.H, s));
+                                                               pb.W, tcoef + r0, hdr, o.grad_X + r0 * pb.H, s));
         }
         {   // grad_W_acc (+)= s P^T X_c
             GemmArgs a = base_args(hdr);
@@ -520,14 +527,18 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                                              grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles), s,
                                              form.pair));
         }
-        // grad_W_acc[y_i] -= s X[i] for the chunk's valid rows, exactly, in row order
+        // grad_W_acc[y_i] += s c_i X[i] for the chunk's valid rows, exactly, in row order
         for (int64_t k = 0; k < p.label_blocks_per_chunk; ++k) {
             if (rows - k * LABEL_BLOCK <= 0) break;
             const int64_t blk = c * p.label_blocks_per_chunk + k;
             LCE_LAUNCH(PK_OTHER, launch_onehot_scatter(keys + blk * LABEL_BLOCK, runs + blk * LABEL_BLOCK,
-                                                       nrun + blk, pb.X + r0 * pb.H, pb.H, hdr, o.grad_W_acc,
-                                                       o.grad_W, last && o.grad_W != nullptr, 4 * sm_count(), s));
+                                                       nrun + blk, pb.X + r0 * pb.H, tcoef + r0, pb.H, hdr,
+                                                       o.grad_W_acc, o.grad_W, lcsum, last && o.grad_W != nullptr,
+                                                       4 * sm_count(), s));
         }
+        // grad_b (after the scatter: the last chunk adds the target entries' sums per label)
+        if (gb)
+            LCE_LAUNCH(PK_OTHER, launch_grad_b(gb, mt * 4, pb.V, hdr, lcsum, o.grad_b_acc, o.grad_b, first, last, s));
         return LCE_OK;
     };
 

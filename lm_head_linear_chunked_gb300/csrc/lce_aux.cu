@@ -16,6 +16,7 @@ namespace lce {
 namespace {
 
 constexpr float LN2_F = 0.6931471805599453f;
+constexpr float LOG2E_F = 1.4426950408889634f;
 
 // Labels must lie in [0, V) or equal ignore_index (cross_entropy's contract).
 // Counts the valid rows; a bad label raises the status bit and is not counted.
@@ -62,8 +63,11 @@ __global__ void scale_kernel(WsHeader* hdr, float grad_scale, const float* d_gra
     if (n_valid_out) *n_valid_out = static_cast<int64_t>(nv);
 }
 
-// lse_i = (M + log2 S) ln 2, where (M, S) merges the per-half-tile partial
-// (max, sum of 2^(t - max)) pairs of row i.  Each row's partial list is cut
+// lse_i = (M + log2(S + T)) ln 2, where (M, S) merges the per-half-tile
+// partial (max, sum of 2^(t - max) over the non-target columns) pairs of row
+// i and T = 2^(z_t log2 e - M) is the target's term (0 for an ignored row).
+// The target entry's gradient coefficient is c_i = p - 1 = -S / (S + T),
+// which has no cancellation however close p is to 1.  Each row's partial list is cut
 // into 32 contiguous parts, each merged in order by one thread (S <- S
 // 2^(M - M') + s_t 2^(m_t - M') when a larger max m_t = M' arrives, else
 // S <- S + s_t 2^(m_t - M)).  The 32 part results are merged by a fixed
@@ -72,7 +76,10 @@ __global__ void scale_kernel(WsHeader* hdr, float grad_scale, const float* d_gra
 // through shared memory.  The tree depends only on the partial count, so lse
 // does not depend on the chunk size.  A block holds 8 rows: the 8 lanes of a
 // part read 8 consecutive rows of a partial, one 32-byte sector.  Row loss =
-// lse_i - z[i, y_i] for valid rows, else 0.
+// lse_i - z[i, y_i] for valid rows, 0 for ignored rows, NaN for a label
+// outside [0, V).  Without pm (the recompute path) every partial is a plain
+// sum of the row's non-target P (max 0: the merge adds them exactly as
+// sums), and only c_i = -S is written.
 __device__ __forceinline__ void merge_partial(float& M, float& S, float m, float s) {
     if (m > M) {
         S = S * exp2f(M - m) + s;
@@ -85,8 +92,8 @@ __device__ __forceinline__ void merge_partial(float& M, float& S, float m, float
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
                                                       int64_t n_pt, int64_t ldp, int64_t rows,
                                                       const float* __restrict__ zt, const int64_t* __restrict__ y,
-                                                      int64_t ignore_index, float* __restrict__ lse,
-                                                      float* __restrict__ row_loss) {
+                                                      int64_t ignore_index, int64_t V, float* __restrict__ lse,
+                                                      float* __restrict__ row_loss, float* __restrict__ tcoef) {
     __shared__ float wm[8][8], wsum[8][8];  // [warp][row of the block]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int part = warp * 4 + (lane >> 3);
@@ -101,13 +108,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
             float m8[8], s8[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                m8[k] = pm[(t + k) * ldp + r];
+                m8[k] = pm ? pm[(t + k) * ldp + r] : 0.f;
                 s8[k] = ps[(t + k) * ldp + r];
             }
 #pragma unroll
             for (int k = 0; k < 8; ++k) merge_partial(M, S, m8[k], s8[k]);
         }
-        for (; t < t1; ++t) merge_partial(M, S, pm[t * ldp + r], ps[t * ldp + r]);
+        for (; t < t1; ++t) merge_partial(M, S, pm ? pm[t * ldp + r] : 0.f, ps[t * ldp + r]);
     }
 #pragma unroll
     for (int o = 8; o <= 16; o <<= 1) {
@@ -135,9 +142,18 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     for (int step = 1; step < 8; step <<= 1)
 #pragma unroll
         for (int w = 0; w < 8; w += 2 * step) merge_partial(m[w], sv[w], m[w + step], sv[w + step]);
-    const float l = (m[0] + log2f(sv[0])) * LN2_F;
+    const int64_t yv = y[r];
+    const bool valid = yv != ignore_index && yv >= 0 && yv < V;
+    if (!pm) {
+        if (tcoef) tcoef[r] = valid ? -sv[0] : 0.f;
+        return;
+    }
+    const float T = valid ? exp2f(zt[r] * LOG2E_F - m[0]) : 0.f;
+    const float St = sv[0] + T;
+    const float l = (m[0] + log2f(St)) * LN2_F;
     lse[r] = l;
-    if (row_loss) row_loss[r] = (y[r] != ignore_index) ? l - zt[r] : 0.f;
+    if (row_loss) row_loss[r] = valid ? l - zt[r] : (yv == ignore_index ? 0.f : __int_as_float(0x7FC00000));
+    if (tcoef) tcoef[r] = valid ? -sv[0] / St : 0.f;
 }
 
 __global__ void __launch_bounds__(256) p_rescale_kernel(uint16_t* __restrict__ P, int64_t ldg, int64_t rows,
@@ -292,7 +308,9 @@ __global__ void gather_f16_kernel(const uint16_t* __restrict__ X_chunk, int64_t 
 }
 
 // loss = sum of row losses / n_valid.  One block; the summation order
-// depends on N only, so the result does not depend on the chunk size.
+// depends on N only, so the result does not depend on the chunk size.  A
+// device error raised earlier in the call (a bad label, a timed-out wait)
+// makes the loss NaN, so the error also shows in the output itself.
 __global__ void loss_kernel(const float* __restrict__ row_loss, int64_t N, const WsHeader* hdr,
                             float* loss, int64_t* n_valid_out, int sum_reduction) {
     __shared__ double red[1024];
@@ -306,7 +324,9 @@ __global__ void loss_kernel(const float* __restrict__ row_loss, int64_t N, const
     }
     if (threadIdx.x == 0) {
         const unsigned long long nv = hdr->n_valid;
-        if (sum_reduction)
+        if (hdr->status != 0)
+            *loss = __int_as_float(0x7FC00000);
+        else if (sum_reduction)
             *loss = static_cast<float>(red[0]);
         else
             *loss = nv ? static_cast<float>(red[0] / static_cast<double>(nv)) : 0.f;
@@ -315,10 +335,11 @@ __global__ void loss_kernel(const float* __restrict__ row_loss, int64_t N, const
 }
 
 // grad_b_acc (+)= s * sum over the chunk's partial column sums of P (fixed
-// order); on the last chunk the one-hot part, -s * (count of label v), is
-// subtracted exactly and grad_b = bf16(grad_b_acc).
+// order; P has no target entries); on the last chunk the target entries'
+// part, s * (sum of c_i over the rows with label v, summed by the scatter
+// kernels in a fixed order), is added and grad_b = bf16(grad_b_acc).
 __global__ void grad_b_kernel(const float* __restrict__ gb_part, int64_t parts, int64_t V,
-                              const WsHeader* hdr, const int* __restrict__ label_counts, float* grad_b_acc,
+                              const WsHeader* hdr, const float* __restrict__ label_csum, float* grad_b_acc,
                               uint16_t* grad_b, int first, int last) {
     const int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     if (v >= V) return;
@@ -326,7 +347,7 @@ __global__ void grad_b_kernel(const float* __restrict__ gb_part, int64_t parts, 
     for (int64_t p = 0; p < parts; ++p) t += gb_part[p * V + v];
     const float s = hdr->scale;
     float a = first ? s * t : fmaf(s, t, grad_b_acc[v]);
-    if (last) a = fmaf(-s, static_cast<float>(label_counts[v]), a);
+    if (last) a = fmaf(s, label_csum[v], a);
     grad_b_acc[v] = a;
     if (last && grad_b) {
         __nv_bfloat16 h = __float2bfloat16_rn(a);
@@ -405,29 +426,33 @@ __global__ void __launch_bounds__(1024) label_sort_kernel(const int64_t* __restr
 }
 
 
-// The one-hot part of grad_W for one sorted block of a chunk:
-//   grad_W_acc[v, :] -= s * sum over the block's rows i with y_i = v of X[i, :]
+// The target entries' part of grad_W for one sorted block of a chunk:
+//   grad_W_acc[v, :] += s * sum over the block's rows i with y_i = v of c_i X[i, :]
+// (c_i = p_{i,y_i} - 1, the entry the tensor-core products leave out).
 // Work items are (run of equal labels, 512-column slab).  Within an item,
 // 64 threads own 8 columns each and four row groups take every fourth row
 // of the run in row order; the four partial sums are added in a fixed
 // order, so the result is the same on every call.  Runs have distinct
 // labels, so no two items touch the same grad_W elements.  With write_bf16
-// the updated elements' bf16 cast is rewritten too.
-__device__ __forceinline__ void add_bf16x8(float (&sum)[8], const uint4 w) {
+// the updated elements' bf16 cast is rewritten too.  With label_csum, the
+// first slab's item also adds the run's sum of c_i to label_csum[v] (lanes
+// of warp 0 take every 32nd row, then a fixed shuffle tree), for grad_b.
+__device__ __forceinline__ void fma_bf16x8(float (&sum)[8], float c, const uint4 w) {
     const uint32_t q[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        sum[2 * k] += __uint_as_float(q[k] << 16);
-        sum[2 * k + 1] += __uint_as_float(q[k] & 0xFFFF0000u);
+        sum[2 * k] = fmaf(c, __uint_as_float(q[k] << 16), sum[2 * k]);
+        sum[2 * k + 1] = fmaf(c, __uint_as_float(q[k] & 0xFFFF0000u), sum[2 * k + 1]);
     }
 }
 
 __global__ void __launch_bounds__(256) onehot_scatter_kernel(const unsigned long long* __restrict__ keys,
                                                              const unsigned long long* __restrict__ runs,
                                                              const int* __restrict__ run_count,
-                                                             const uint16_t* __restrict__ X_chunk, int64_t H,
+                                                             const uint16_t* __restrict__ X_chunk,
+                                                             const float* __restrict__ tcoef, int64_t H,
                                                              const WsHeader* hdr, float* grad_W_acc,
-                                                             uint16_t* grad_W, int write_bf16) {
+                                                             uint16_t* grad_W, float* label_csum, int write_bf16) {
     __shared__ float part[3][64][9];
     const int ct = threadIdx.x & 63, rg = threadIdx.x >> 6;
     const int slabs = static_cast<int>((H + 511) / 512);
@@ -446,17 +471,19 @@ __global__ void __launch_bounds__(256) onehot_scatter_kernel(const unsigned long
             int64_t j = start + rg;
             for (; j + 12 < end; j += 16) {  // four rows of this group in flight
                 uint4 w[4];
+                float c[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int64_t row = static_cast<int64_t>(keys[j + 4 * u] & 0xFFFFFFFFull);
                     w[u] = *reinterpret_cast<const uint4*>(X_chunk + row * H + h);
+                    c[u] = tcoef[row];
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) add_bf16x8(sum, w[u]);
+                for (int u = 0; u < 4; ++u) fma_bf16x8(sum, c[u], w[u]);
             }
             for (; j < end; j += 4) {
                 const int64_t row = static_cast<int64_t>(keys[j] & 0xFFFFFFFFull);
-                add_bf16x8(sum, *reinterpret_cast<const uint4*>(X_chunk + row * H + h));
+                fma_bf16x8(sum, tcoef[row], *reinterpret_cast<const uint4*>(X_chunk + row * H + h));
             }
         }
         if (rg > 0) {
@@ -470,14 +497,14 @@ __global__ void __launch_bounds__(256) onehot_scatter_kernel(const unsigned long
             float* acc = grad_W_acc + static_cast<int64_t>(v) * H + h;
             float4 a0 = *reinterpret_cast<float4*>(acc);
             float4 a1 = *reinterpret_cast<float4*>(acc + 4);
-            a0.x = fmaf(-s, sum[0], a0.x);
-            a0.y = fmaf(-s, sum[1], a0.y);
-            a0.z = fmaf(-s, sum[2], a0.z);
-            a0.w = fmaf(-s, sum[3], a0.w);
-            a1.x = fmaf(-s, sum[4], a1.x);
-            a1.y = fmaf(-s, sum[5], a1.y);
-            a1.z = fmaf(-s, sum[6], a1.z);
-            a1.w = fmaf(-s, sum[7], a1.w);
+            a0.x = fmaf(s, sum[0], a0.x);
+            a0.y = fmaf(s, sum[1], a0.y);
+            a0.z = fmaf(s, sum[2], a0.z);
+            a0.w = fmaf(s, sum[3], a0.w);
+            a1.x = fmaf(s, sum[4], a1.x);
+            a1.y = fmaf(s, sum[5], a1.y);
+            a1.z = fmaf(s, sum[6], a1.z);
+            a1.w = fmaf(s, sum[7], a1.w);
             *reinterpret_cast<float4*>(acc) = a0;
             *reinterpret_cast<float4*>(acc + 4) = a1;
             if (write_bf16) {
@@ -490,6 +517,14 @@ __global__ void __launch_bounds__(256) onehot_scatter_kernel(const unsigned long
                 o.w = *reinterpret_cast<uint32_t*>(&b3);
                 *reinterpret_cast<uint4*>(grad_W + static_cast<int64_t>(v) * H + h) = o;
             }
+        }
+        if (label_csum && item % slabs == 0 && threadIdx.x < 32) {
+            float c = 0.f;
+            for (int64_t jj = start + threadIdx.x; jj < end; jj += 32)
+                c += tcoef[static_cast<int64_t>(keys[jj] & 0xFFFFFFFFull)];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+            if (threadIdx.x == 0) label_csum[v] += c;
         }
         __syncthreads();
     }
@@ -534,13 +569,13 @@ __global__ void scale_grads_kernel(int64_t nx8, int64_t nw8, int64_t V, const fl
 
 // Finishes a split grad_X product: for each compacted row j < n_valid and
 // column h, sum the K slices' partial sums in slice order, then
-// grad_X[crow[j], h] = s (2^-(15+k_W) sum - W[y, h]) as bf16 (the same
+// grad_X[crow[j], h] = s (2^-(15+k_W) sum + c W[y, h]) as bf16 (the same
 // arithmetic as the unsplit epilogue).
 __global__ void gradx_split_reduce_kernel(const float* __restrict__ split_out, int64_t splits, int64_t split_stride,
                                           int64_t H, const int* __restrict__ crow, const int* __restrict__ n_valid,
                                           const int64_t* __restrict__ y, int64_t ignore_index, int64_t V,
-                                          const uint16_t* __restrict__ W, const WsHeader* hdr,
-                                          uint16_t* __restrict__ grad_X_chunk) {
+                                          const uint16_t* __restrict__ W, const float* __restrict__ tcoef,
+                                          const WsHeader* hdr, uint16_t* __restrict__ grad_X_chunk) {
     const float s = hdr->scale;
     const float f = ldexpf(s, -(P_SCALE_EXP + operand_scale_exp(hdr->amax_w_bits)));
     const int64_t nv = *n_valid, h8 = H / 8;
@@ -560,7 +595,9 @@ __global__ void gradx_split_reduce_kernel(const float* __restrict__ split_out, i
         const int64_t r = crow[j];
         const int64_t yr = y[r];
         float w[8];
-        if (yr != ignore_index && yr >= 0 && yr < V) {
+        const bool valid = yr != ignore_index && yr >= 0 && yr < V;
+        const float sc = valid ? s * tcoef[r] : 0.f;
+        if (valid) {
             const uint4 q = *reinterpret_cast<const uint4*>(W + yr * H + h);
             const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -575,8 +612,8 @@ __global__ void gradx_split_reduce_kernel(const float* __restrict__ split_out, i
         uint32_t o[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(fmaf(f, sum[2 * k], -s * w[2 * k]),
-                                                      fmaf(f, sum[2 * k + 1], -s * w[2 * k + 1]));
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(fmaf(f, sum[2 * k], sc * w[2 * k]),
+                                                      fmaf(f, sum[2 * k + 1], sc * w[2 * k + 1]));
             o[k] = *reinterpret_cast<uint32_t*>(&b2);
         }
         *reinterpret_cast<uint4*>(grad_X_chunk + r * H + h) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -681,10 +718,11 @@ cudaError_t launch_label_sort(const int64_t* y, int64_t N, int64_t C, int64_t bl
 }
 
 cudaError_t launch_onehot_scatter(const unsigned long long* keys, const unsigned long long* runs, const int* run_count,
-                                  const uint16_t* X_chunk, int64_t H, const WsHeader* hdr, float* grad_W_acc,
-                                  uint16_t* grad_W, int write_bf16, int grid, cudaStream_t s) {
-    onehot_scatter_kernel<<<grid, 256, 0, s>>>(keys, runs, run_count, X_chunk, H, hdr, grad_W_acc, grad_W,
-                                               write_bf16);
+                                  const uint16_t* X_chunk, const float* tcoef, int64_t H, const WsHeader* hdr,
+                                  float* grad_W_acc, uint16_t* grad_W, float* label_csum, int write_bf16, int grid,
+                                  cudaStream_t s) {
+    onehot_scatter_kernel<<<grid, 256, 0, s>>>(keys, runs, run_count, X_chunk, tcoef, H, hdr, grad_W_acc, grad_W,
+                                               label_csum, write_bf16);
     return cudaGetLastError();
 }
 
@@ -695,12 +733,12 @@ cudaError_t launch_scale(WsHeader* hdr, float grad_scale, const float* d_grad_ou
 }
 
 cudaError_t launch_combine(const float* part_m, const float* part_s, int64_t n_pt, int64_t ldp, int64_t rows,
-                           const float* zt, const int64_t* y, int64_t ignore_index, float* lse, float* row_loss,
-                           cudaStream_t s) {
+                           const float* zt, const int64_t* y, int64_t ignore_index, int64_t V, float* lse,
+                           float* row_loss, float* tcoef, cudaStream_t s) {
     const int threads = 256;  // 8 rows, 32 threads each
     const int64_t blocks = (rows + 7) / 8;
     combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(part_m, part_s, n_pt, ldp, rows, zt, y,
-                                                                      ignore_index, lse, row_loss);
+                                                                      ignore_index, V, lse, row_loss, tcoef);
     return cudaGetLastError();
 }
 
@@ -711,11 +749,11 @@ cudaError_t launch_loss(const float* row_loss, int64_t N, const WsHeader* hdr, f
 }
 
 cudaError_t launch_grad_b(const float* gb_part, int64_t parts, int64_t V, const WsHeader* hdr,
-                          const int* label_counts, float* grad_b_acc, uint16_t* grad_b, int first, int last,
+                          const float* label_csum, float* grad_b_acc, uint16_t* grad_b, int first, int last,
                           cudaStream_t s) {
     const int threads = 256;
     const int64_t blocks = (V + threads - 1) / threads;
-    grad_b_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(gb_part, parts, V, hdr, label_counts,
+    grad_b_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(gb_part, parts, V, hdr, label_csum,
                                                                      grad_b_acc, grad_b, first, last);
     return cudaGetLastError();
 }
@@ -790,12 +828,12 @@ cudaError_t launch_scale_grads(int64_t N, int64_t H, int64_t V, const float* d_g
 
 cudaError_t launch_gradx_split_reduce(const float* split_out, int64_t splits, int64_t split_stride, int64_t H,
                                       const int* crow, const int* n_valid, int64_t max_rows, const int64_t* y,
-                                      int64_t ignore_index, int64_t V, const uint16_t* W, const WsHeader* hdr,
-                                      uint16_t* grad_X_chunk, cudaStream_t s) {
+                                      int64_t ignore_index, int64_t V, const uint16_t* W, const float* tcoef,
+                                      const WsHeader* hdr, uint16_t* grad_X_chunk, cudaStream_t s) {
     const int64_t want = (max_rows * (H / 8) + 255) / 256;
     const int blocks = static_cast<int>(want < 1 ? 1 : (want < 4096 ? want : 4096));
     gradx_split_reduce_kernel<<<blocks, 256, 0, s>>>(split_out, splits, split_stride, H, crow, n_valid, y,
-                                                     ignore_index, V, W, hdr, grad_X_chunk);
+                                                     ignore_index, V, W, tcoef, hdr, grad_X_chunk);
     return cudaGetLastError();
 }
 

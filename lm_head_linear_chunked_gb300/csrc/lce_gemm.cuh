@@ -312,9 +312,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
 
     if constexpr (MODE == MODE_LSE) {
         // Two passes over the tile's TMEM row.  Pass 1: the tile max of
-        // t = z log2(e) and the target logit.  Pass 2: s = sum 2^(t - max),
-        // and with a.g set, E = fp16(2^(t - max) * 2^P_SCALE_EXP) for the
-        // backward (rescaled to P once lse is known).
+        // t = z log2(e) and the target logit.  Pass 2: s = sum 2^(t - max)
+        // over the columns other than the row's target (the combine kernel
+        // adds the target's term), and with a.g set, E = fp16(2^(t - max) *
+        // 2^P_SCALE_EXP) for the backward (rescaled to P once lse is known),
+        // 0 at the target.
         const int64_t yr = row_ok ? a.y[row] : a.ignore_index;
         // The max is taken over z and scaled once: rounding is monotone, so
         // max(z) * log2(e) rounds to the same float as max(z * log2(e)).
@@ -354,7 +356,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
             tmem_load_32cols(taddr + 32 * j, v);
             const int nv = static_cast<int>(min64(32, a.N - c0));
             if (a.bias) add_bias32(v, a.bias + c0, nv);
-            if (nv == 32) {  // a whole chunk (all but the vocabulary's last): no per-column checks
+            const int64_t d = yr - c0;
+            const int kk = (d >= 0 && d < 32) ? static_cast<int>(d) : -1;  // the row's target column here
+            const bool tgt = __any_sync(0xFFFFFFFFu, kk >= 0);
+            if (nv == 32 && !tgt) {  // a whole chunk without a target: no per-column checks
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const float e = fast_exp2(v[i] * LOG2E_F - mx);
@@ -364,7 +369,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float e = (i < nv) ? fast_exp2(v[i] * LOG2E_F - mx) : 0.f;
+                    const float e = (i < nv && i != kk) ? fast_exp2(v[i] * LOG2E_F - mx) : 0.f;
                     sm += e;
                     v[i] = e * P_SCALE;
                 }
@@ -381,9 +386,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
             if (got) a.zt[row] = zt;
         }
     } else if constexpr (MODE == MODE_G) {
+        // P = exp(z - lse) without the target entry, and the half tile's sum
+        // of it (the combine kernel turns the row's sum into c = -sum P)
         const int64_t yr = row_ok ? a.y[row] : a.ignore_index;
         const bool valid = row_ok && yr != a.ignore_index;
         const float lse2 = row_ok ? a.lse[row] * LOG2E_F : 0.f;
+        float se = 0.f;
 #pragma unroll 1
         for (int j = j0; j < j0 + BN / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
@@ -392,10 +400,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
             tmem_load_32cols(taddr + 32 * j, v);
             const int nv = static_cast<int>(min64(32, a.N - c0));
             if (a.bias) add_bias32(v, a.bias + c0, nv);
+            const int64_t d = yr - c0;
+            const int kk = (d >= 0 && d < 32) ? static_cast<int>(d) : -1;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const float p = fast_exp2(fmaf(v[i], LOG2E_F, -lse2));
-                v[i] = (valid && i < nv) ? p : 0.f;
+                v[i] = (valid && i < nv && i != kk) ? p : 0.f;
+                se += v[i];
             }
             if (prow >= 0) {
                 float ps[32];
@@ -411,6 +422,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) release_acc<PAIR>(empty_bar);
+        if (row_ok && a.part_s) a.part_s[(2 * static_cast<int64_t>(n) + half) * a.ldp + row] = se;
     } else if constexpr (MODE == MODE_GRADX) {
       if (a.k_splits > 1) {
         // one K slice of a split product: the raw fp32 partial sums, finished
@@ -432,12 +444,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         __syncwarp();
         if (lane == 0) release_acc<PAIR>(empty_bar);
       } else {
-        // grad_X[i] = s (sum_v P[i,v] W[v] - W[y_i]); P rows of ignored rows are 0
+        // grad_X[i] = s (sum_v P[i,v] W[v] + c_i W[y_i]), P without the target
+        // entry, c_i = p_{i,y_i} - 1; P rows of ignored rows are 0
         const float s = *a.scale;
         const float f = ldexpf(s, -(P_SCALE_EXP + operand_scale_exp(*a.b_amax_bits)));
         const int64_t orow = (a.row_map && row_ok) ? static_cast<int64_t>(a.row_map[row]) : row;  // chunk row
         const int64_t yr = row_ok ? a.y[orow] : a.ignore_index;
         const bool valid = row_ok && yr != a.ignore_index && yr >= 0 && yr < a.V;
+        const float sc = valid ? s * a.tcoef[orow] : 0.f;
         const uint16_t* wy = a.w_rows + (valid ? yr : 0) * a.ldw;
 #pragma unroll 1
         for (int j = j0; j < j0 + BN / 64; ++j) {
@@ -452,7 +466,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
                     for (int i = 0; i < 32; ++i) w[i] = 0.f;
                     add_bias32(w, wy + c0, 32);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = fmaf(f, v[i], -s * w[i]);
+                    for (int i = 0; i < 32; ++i) v[i] = fmaf(f, v[i], sc * w[i]);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= f;

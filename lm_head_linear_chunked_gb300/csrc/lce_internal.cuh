@@ -16,12 +16,24 @@ enum GemmMode : int {
     MODE_PLAIN_KK = 0,  // D = A B^T,  A [M,K], B [N,K]        (both K-major)
     MODE_PLAIN_KM = 1,  // D = A B,    A [M,K], B [K,N]        (B MN-major)
     MODE_PLAIN_MM = 2,  // D = A^T B,  A [K,M], B [K,N]        (both MN-major)
-    MODE_LSE = 3,       // logits X_c W^T -> per-row partial (max, sum exp), target logit,
-                        //   optionally E = 2^(t - tile max) for the backward
-    MODE_G = 4,         // logits X_c W^T -> P = softmax (fp16, scaled by 2^P_SCALE_EXP), bias column sums
-    MODE_GRADX = 5,     // grad_X_c = s * (P W - W[y])           (fp16 operands, bf16 out)
+    MODE_LSE = 3,       // logits X_c W^T -> per-row partial (max, sum exp over the non-target columns),
+                        //   target logit, optionally E = 2^(t - tile max) (0 at the target) for the backward
+    MODE_G = 4,         // logits X_c W^T -> P = softmax without the target entry (fp16, scaled by
+                        //   2^P_SCALE_EXP), per-row partial sums of P, bias column sums
+    MODE_GRADX = 5,     // grad_X_c = s * (P W + c W[y])         (fp16 operands, bf16 out)
     MODE_GRADW = 6,     // grad_W_acc (+)= s * P^T X_c           (fp16 operands, fp32 accumulator, bf16 cast)
 };
+
+// The softmax's target entry is never a tensor-core operand.  In a peaked
+// softmax (a trained head puts p ~ 0.9-0.99 on the label) a 16-bit p would
+// carry an error of 2^-11 p against the gradient entry p - 1, which is then
+// small.  So every P the GEMMs read has a zero at (i, y_i), and the target
+// column's gradient s * c_i with c_i = p_{i,y_i} - 1 is applied exactly, in
+// fp32, by the grad_X epilogue (+ s c_i W[y_i]), the label-sorted scatter
+// (grad_W_acc[y_i] += s c_i x_i) and the grad_b kernel.  The forward gets
+// c_i without cancellation as -S'/(S' + T), S' the row's sum of exponentials
+// over the other columns and T the target's; the recompute path sums the
+// other columns' p instead.
 
 // Tile shape: 128 rows (TMEM lanes) x 256 columns (fp32 TMEM columns),
 // 64-element (128-byte) K slices, a 4-deep shared-memory ring.
@@ -118,14 +130,17 @@ struct GemmArgs {
     int64_t ignore_index;
     const uint16_t* bias;  // nullable
     float* part_m;     // [2 n_tiles, ldp] per-row max of each 128-column half tile (base-2 units)
-    float* part_s;     // [2 n_tiles, ldp] per-row sum of 2^(t - max) over the half tile
+    float* part_s;     // [2 n_tiles, ldp] MODE_LSE: per-row sum of 2^(t - max) over the half tile's columns
+                       //   other than the row's target; MODE_G: per-row sum of P over the same columns
     float* zt;         // [chunk rows] target logit
     int64_t ldp;
     const float* lse;  // this chunk's first row
     uint16_t* g;       // P [chunk rows, ldg] bf16
     int64_t ldg;
     float* gb_part;    // [m_tiles * 4, V] column sums of P (nullable)
-    // MODE_GRADX: the one-hot part, -W[y_i], is applied exactly in the epilogue
+    // MODE_GRADX: the target column's part, c_i W[y_i], is applied exactly in the
+    // epilogue (tcoef: c_i of this chunk's rows, indexed by chunk row)
+    const float* tcoef;
     const uint16_t* w_rows;
     int64_t ldw;
     int64_t V;
@@ -198,21 +213,28 @@ cudaError_t launch_label_sort(const int64_t* y, int64_t N, int64_t C, int64_t bl
                               int64_t n_blocks, int64_t V, int64_t ignore_index,
                               unsigned long long* keys, unsigned long long* runs, int* run_count,
                               cudaStream_t s);
+// grad_W_acc[v] += s * sum of c_i X[i] over the block's rows with y_i = v
+// (tcoef: c_i of the chunk's rows); with label_csum, also
+// label_csum[v] += sum of those c_i (for grad_b).
 cudaError_t launch_onehot_scatter(const unsigned long long* keys, const unsigned long long* runs,
-                                  const int* run_count, const uint16_t* X_chunk, int64_t H,
+                                  const int* run_count, const uint16_t* X_chunk, const float* tcoef, int64_t H,
                                   const WsHeader* hdr, float* grad_W_acc, uint16_t* grad_W,
-                                  int write_bf16, int grid, cudaStream_t s);
+                                  float* label_csum, int write_bf16, int grid, cudaStream_t s);
 // s = grad_scale * grad_output / n_valid (mean), or grad_scale * grad_output (sum_reduction).
 cudaError_t launch_scale(WsHeader* hdr, float grad_scale, const float* d_grad_output,
                          int64_t* n_valid_out, bool sum_reduction, cudaStream_t s);
+// Per row of a chunk: merges the partials into lse; row loss lse - z_t (NaN
+// for a label outside [0, V) that is not ignore_index); tcoef (nullable):
+// c = p_target - 1.  With part_m == nullptr the partials are plain sums of
+// the non-target P (the recompute path) and only tcoef = -sum is written.
 cudaError_t launch_combine(const float* part_m, const float* part_s, int64_t n_vt, int64_t ldp,
-                           int64_t rows, const float* zt, const int64_t* y, int64_t ignore_index,
-                           float* lse, float* row_loss, cudaStream_t s);
+                           int64_t rows, const float* zt, const int64_t* y, int64_t ignore_index, int64_t V,
+                           float* lse, float* row_loss, float* tcoef, cudaStream_t s);
 // loss = mean (or, with sum_reduction, sum) of the row losses of the valid rows.
 cudaError_t launch_loss(const float* row_loss, int64_t N, const WsHeader* hdr, float* loss,
                         int64_t* n_valid_out, bool sum_reduction, cudaStream_t s);
 cudaError_t launch_grad_b(const float* gb_part, int64_t parts, int64_t V, const WsHeader* hdr,
-                          const int* label_counts, float* grad_b_acc, uint16_t* grad_b, int first,
+                          const float* label_csum, float* grad_b_acc, uint16_t* grad_b, int first,
                           int last, cudaStream_t s);
 cudaError_t launch_wait_probe(unsigned* status, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_p_rescale(uint16_t* P, int64_t ldg, int64_t rows, int64_t V, const float* pm, int64_t ldp,
@@ -229,8 +251,8 @@ cudaError_t launch_gather_f16(const uint16_t* X_chunk, int64_t H, const int* cro
                               int64_t ldg, cudaStream_t s);
 cudaError_t launch_gradx_split_reduce(const float* split_out, int64_t splits, int64_t split_stride, int64_t H,
                                       const int* crow, const int* n_valid, int64_t max_rows, const int64_t* y,
-                                      int64_t ignore_index, int64_t V, const uint16_t* W, const WsHeader* hdr,
-                                      uint16_t* grad_X_chunk, cudaStream_t s);
+                                      int64_t ignore_index, int64_t V, const uint16_t* W, const float* tcoef,
+                                      const WsHeader* hdr, uint16_t* grad_X_chunk, cudaStream_t s);
 cudaError_t launch_amax(const uint16_t* x, int64_t n, unsigned* amax_bits, cudaStream_t s);
 cudaError_t launch_to_f16_scaled(const uint16_t* x, int64_t n, const unsigned* amax_bits, uint16_t* out,
                                  cudaStream_t s);

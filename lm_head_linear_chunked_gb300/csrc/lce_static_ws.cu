@@ -71,7 +71,18 @@ extern "C" lce_status_t lce_forward_static_ws(int64_t N, int64_t H, int64_t V, c
     st = scratch_address(&scratch);
     if (st != LCE_OK) return st;
     // lce_forward clears the status word and the valid-row count at the start
-    // of every call; everything else it reads from the scratch it writes first.
+    // of every call.  The other scratch it reads (per-row partials and target
+    // logits) is written earlier in the same call unless the call finds an
+    // error on the device: a label outside [0, V) gets a NaN row loss without
+    // reading a target logit, and any device error makes the loss NaN and
+    // shows in lce_static_ws_check_status.
     return lce_forward(N, H, V, X, W, b, y, ignore_index, rows, loss, lse, n_valid, scratch,
                        LCE_STATIC_SCRATCH_BYTES, stream);
+}
+
+extern "C" lce_status_t lce_static_ws_check_status(lce_stream_t stream) {
+    void* scratch = nullptr;
+    const lce_status_t st = scratch_address(&scratch);
+    if (st != LCE_OK) return st;
+    return lce_check_status(scratch, stream);
 }

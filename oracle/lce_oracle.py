@@ -234,6 +234,53 @@ def rows_grad_X(X_rows, W, b, y_rows, lse_rows, s: float,
     return G @ W
 
 
+def grad_W_columns(X, W, b, y, h0: int, h1: int, ignore_index: int = IGNORE_INDEX,
+                   grad_scale: float = 1.0, grad_output: float = 1.0, block_rows: int = 128,
+                   threads: Optional[int] = None) -> dict:
+    """Columns h0:h1 of grad_W = G^T X over ALL rows (reduction "mean"),
+    with the whole problem's lse, loss and grad_b.
+
+    Each block of rows gets its logits, its lse and its G (the definitions
+    above, row by row), and contributes G^T X[:, h0:h1]; the blocks'
+    contributions are added in row order.  This costs the full 2 N H V of
+    logits but holds only one block's, so the FP32 accumulation over many
+    chunks can be checked on all rows of a large problem."""
+    X, W, b = as_f64(X), as_f64(W), as_f64(b)
+    y = np.asarray(y, dtype=np.int64)
+    N, V = X.shape[0], W.shape[0]
+    check_labels(y, V, ignore_index)
+    n_valid = count_valid(y, ignore_index)
+    s = grad_scale_per_row(grad_scale, grad_output, n_valid)
+    blocks = _blocks(N, block_rows)
+    lse = np.empty(N)
+    zt = np.zeros(N)
+    slice_parts = [None] * len(blocks)
+    bias_parts = [None] * len(blocks)
+
+    def one(j):
+        r0, r1 = blocks[j]
+        z = logits(X[r0:r1], W, b)
+        lse[r0:r1] = logsumexp_rows(z)
+        yy = y[r0:r1]
+        kept = np.nonzero(yy != ignore_index)[0]
+        zt[r0 + kept] = z[kept, yy[kept]]
+        G = softmax_minus_onehot(z, lse[r0:r1], yy, s, ignore_index)
+        slice_parts[j] = G.T @ X[r0:r1, h0:h1]
+        bias_parts[j] = G.sum(axis=0)
+
+    with _pool(threads) as ex:
+        list(ex.map(one, range(len(blocks))))
+    cols = np.zeros((V, h1 - h0))
+    grad_b = np.zeros(V)
+    for j in range(len(blocks)):          # fixed order
+        cols += slice_parts[j]
+        grad_b += bias_parts[j]
+    ok = valid_mask(y, ignore_index)
+    loss = float((lse[ok] - zt[ok]).sum()) / n_valid if n_valid else 0.0
+    return {"grad_W_cols": cols, "grad_b": grad_b if b is not None else None, "lse": lse, "loss": loss,
+            "n_valid": n_valid}
+
+
 def target_logits(X, W, b, y, ignore_index: int = IGNORE_INDEX,
                   block_rows: int = 65536) -> np.ndarray:
     """z[i, y[i]] for every row (NaN for ignored rows): N*H work, no full logits."""

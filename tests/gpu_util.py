@@ -68,14 +68,20 @@ def fp16_acc_bound(X, W, b, y, lse, s, ignore_index=-100):
     at most twice (the fused path stores 2^(t - tile max) in fp16 and rescales
     it to P in fp16; each rounding is <= 2^-11 relative), so
     |err[v,h]| <= s * 2^-10 * sum_i p[i,v] |x[i,h]|, plus 1e-5 * max|ref| for
-    fp32 accumulation and the approximate exp.
-    Used for shapes outside the five workloads (e.g. V = 8, one row), where
-    a softmax with few classes puts O(1) probabilities in single entries."""
+    fp32 accumulation and the approximate exp.  The target entries p[i, y_i]
+    are not 16-bit operands (their gradient is applied in fp32), so they are
+    left out of the sum.
+    Used for shapes outside the five workloads and the peaked-softmax cases
+    (e.g. V = 8, one row), where a softmax with few classes puts O(1)
+    probabilities in single non-target entries."""
     import oracle
     Xf, Wf, bf = oracle.as_f64(X), oracle.as_f64(W), oracle.as_f64(b)
     z = oracle.logits(Xf, Wf, bf)
     p = np.exp(z - np.asarray(lse)[:, None])
-    p[np.asarray(y) == ignore_index] = 0.0
+    y = np.asarray(y)
+    p[y == ignore_index] = 0.0
+    rows = np.nonzero(y != ignore_index)[0]
+    p[rows, y[rows]] = 0.0
     return s * 2.0 ** -10 * (p.T @ np.abs(Xf))
 
 

@@ -367,6 +367,31 @@ def pin_row_sampled_pieces(orc):
     return fails
 
 
+def pin_column_slice(orc):
+    """grad_W_columns against torch CPU float64 cross_entropy + autograd:
+    the chosen columns of grad_W (all rows), grad_b, lse and the loss."""
+    import torch
+    fails = []
+    for (h0, h1, block) in ((2, 5, 3), (0, 8, 100), (7, 8, 1)):
+        X, W, b, y = tiny_problem(23, N=11, H=8, V=13, ignore=(0, 6))
+        out = orc.grad_W_columns(X, W, b, y, h0, h1, grad_scale=0.7, grad_output=1.3, block_rows=block)
+        Xt = torch.tensor(X, requires_grad=True)
+        Wt = torch.tensor(W, requires_grad=True)
+        bt = torch.tensor(b, requires_grad=True)
+        z = Xt @ Wt.T + bt
+        loss = torch.nn.functional.cross_entropy(z, torch.tensor(y), ignore_index=IGN)
+        (loss * 0.7 * 1.3).backward()
+        if not _close(out["grad_W_cols"], Wt.grad.numpy()[:, h0:h1], 1e-11):
+            fails.append(f"column slice {h0}:{h1} grad_W")
+        if not _close(out["grad_b"], bt.grad.numpy(), 1e-11):
+            fails.append("column slice grad_b")
+        if not _close(out["lse"], torch.logsumexp(z, 1).detach().numpy(), 1e-12):
+            fails.append("column slice lse")
+        if abs(out["loss"] - loss.item()) > 1e-12 * abs(loss.item()):
+            fails.append("column slice loss")
+    return fails
+
+
 def pin_bf16_decode(orc):
     """bf16 bit patterns decode to the values their IEEE fields define:
     sign, 8 exponent bits (bias 127), 7 fraction bits; subnormals 0.f 2^-126.
@@ -382,7 +407,7 @@ def pin_bf16_decode(orc):
     return fails
 
 
-ALL_PINS = [pin_bf16_decode, pin_zero_weight_closed_form, pin_rows_sum_to_zero, pin_ignored_rows,
+ALL_PINS = [pin_bf16_decode, pin_column_slice, pin_zero_weight_closed_form, pin_rows_sum_to_zero, pin_ignored_rows,
             pin_finite_differences, pin_shift_invariance, pin_row_permutation,
             pin_torch_cross_entropy, pin_torch_cross_entropy_sum, pin_finite_differences_sum,
             pin_single_class, pin_no_valid_rows,

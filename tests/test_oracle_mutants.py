@@ -45,6 +45,8 @@ MUTANTS = {
                                "        return a.view(np.float16).astype(np.float64)\n"),
     "bf16_decode_drops_sign": ("        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)\n",
                                "        return ((a.astype(np.uint32) & 0x7FFF) << 16).view(np.float32).astype(np.float64)\n"),
+    "column_slice_offset": ("        slice_parts[j] = G.T @ X[r0:r1, h0:h1]\n",
+                            "        slice_parts[j] = G.T @ X[r0:r1, h0 + 1:h1 + 1]\n"),
     "target_logit_wrong_column": ("        zt[r0:r1][ok] = z[np.nonzero(ok)[0], yy[ok]]\n",
                                   "        zt[r0:r1][ok] = z[np.nonzero(ok)[0], 0]\n"),
 }
