@@ -189,6 +189,10 @@ __device__ __forceinline__ float warp_column_sums(float (&g)[32], int lane) {
     return g[0];
 }
 
+__device__ __forceinline__ bool gradw_nothing_to_add(const GemmArgs& a) {
+    return a.dyn_rows && *a.dyn_rows == 0 && !a.acc_first && !a.write_bf16;
+}
+
 // Whether the grad_W epilogue reads the accumulator's old values into the
 // SM (the read-modify-write path): not on the first chunk, and not when the
 // tile is added into the accumulator at L2 by a TMA reduce.
@@ -597,6 +601,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const __grid_constant__ CUtensorMap map_c, const GemmArgs args) {
     using T = ModeTraits<MODE>;
+    // A chunk without valid rows adds nothing to the grad_W accumulator: unless
+    // its tiles overwrite the accumulator (first chunk) or write its bf16 cast
+    // (last chunk), every CTA (both of a pair alike) leaves at once.
+    if (MODE == MODE_GRADW && gradw_nothing_to_add(args)) return;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle needs 1024-byte alignment

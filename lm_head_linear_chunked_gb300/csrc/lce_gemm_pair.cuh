@@ -62,6 +62,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                      const __grid_constant__ CUtensorMap map_c, const GemmArgs args) {
     using T = ModeTraits<MODE>;
+    // A chunk without valid rows adds nothing to the grad_W accumulator: unless
+    // its tiles overwrite the accumulator (first chunk) or write its bf16 cast
+    // (last chunk), every CTA (both of a pair alike) leaves at once.
+    if (MODE == MODE_GRADW && gradw_nothing_to_add(args)) return;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle needs 1024-byte alignment
