@@ -82,7 +82,9 @@ typedef enum {
     LCE_ERR_WORKSPACE = 3,     /* ws_bytes smaller than lce_workspace_size() */
     LCE_ERR_LABEL_RANGE = 4,   /* device: a label outside [0,V) and != ignore_index */
     LCE_ERR_TIMEOUT = 5,       /* device: a pipeline wait exceeded its time limit */
-    LCE_ERR_CUDA = 6           /* a CUDA runtime call or launch failed */
+    LCE_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed */
+    LCE_ERR_BOUNDS = 7         /* device, bounds-checking build only: an index or TMA coordinate fell
+                                  outside its buffer (the access was skipped) */
 } lce_status_t;
 
 /* Which entry point a workspace is sized for.  LCE_WS_FUSED is the size for
@@ -200,9 +202,18 @@ LCE_API lce_status_t lce_scale_grads(int64_t N, int64_t H, int64_t V, const floa
                              const float* grad_b_acc, lce_bf16* grad_b, lce_stream_t stream);
 
 /* Synchronises `stream`, then returns the device status of the last call
- * that used workspace `ws` (LCE_OK, LCE_ERR_LABEL_RANGE, LCE_ERR_TIMEOUT),
- * or LCE_ERR_CUDA if the stream reported an error.  A call that found an
- * error on the device also writes NaN to its loss. */
+ * that used workspace `ws` (LCE_OK, LCE_ERR_LABEL_RANGE, LCE_ERR_TIMEOUT,
+ * or LCE_ERR_BOUNDS from the bounds-checking build), or LCE_ERR_CUDA if the
+ * stream reported an error.  A call that found an error on the device also
+ * writes NaN to its loss.
+ *
+ * Bounds-checking build.  The same sources compiled with LCE_DEBUG give
+ * liblce_debug.so, with the same entry points: there every kernel checks
+ * the indices it computes (row maps, sorted label keys, chunk rows, partial
+ * and workspace offsets) and the coordinates of its TMA stores against the
+ * buffers they address, and a check that fails skips the access and
+ * raises LCE_ERR_BOUNDS instead of touching memory outside the buffer.  The
+ * release library compiles these checks out. */
 LCE_API lce_status_t lce_check_status(const void* ws, lce_stream_t stream);
 
 /* Static, human-readable name of a status code. */

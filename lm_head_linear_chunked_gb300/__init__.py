@@ -32,10 +32,13 @@ __all__ = [
 IGNORE_INDEX = -100
 WS_FORWARD, WS_BACKWARD, WS_FUSED, WS_FUSED_MIN = 0, 1, 2, 3
 STATUS = {0: "LCE_OK", 1: "LCE_ERR_INVALID_ARG", 2: "LCE_ERR_UNSUPPORTED", 3: "LCE_ERR_WORKSPACE",
-          4: "LCE_ERR_LABEL_RANGE", 5: "LCE_ERR_TIMEOUT", 6: "LCE_ERR_CUDA"}
+          4: "LCE_ERR_LABEL_RANGE", 5: "LCE_ERR_TIMEOUT", 6: "LCE_ERR_CUDA", 7: "LCE_ERR_BOUNDS"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-library_path = os.path.join(_HERE, "liblce.so")
+# LCE_LIBRARY=debug in the environment loads the bounds-checking build
+# (liblce_debug.so: the same entry points, every kernel checking its indices
+# and reporting a failed check as LCE_ERR_BOUNDS) instead of liblce.so.
+library_path = os.path.join(_HERE, "liblce_debug.so" if os.environ.get("LCE_LIBRARY") == "debug" else "liblce.so")
 
 _lib = None
 _lock = threading.Lock()

@@ -1,4 +1,7 @@
-"""Builds liblce.so, the library behind include/lce.h, in-tree for sm_103a.
+"""Builds liblce.so, the library behind include/lce.h, in-tree for sm_103a,
+and its bounds-checking twin liblce_debug.so (the same sources compiled with
+LCE_DEBUG: every kernel checks its computed indices and TMA store
+coordinates and reports a failed check as LCE_ERR_BOUNDS).
 
 Each .cu file is compiled separately (in parallel) with nvcc and linked
 into one shared library with the CUDA runtime linked statically, so that
@@ -19,6 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblce.so")
+LIB_DEBUG = os.path.join(PKG, "liblce_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -41,43 +45,62 @@ def _deps() -> list[str]:
     return files + [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)] + [__file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def _variant(debug: bool):
+    """(library path, object folder, extra nvcc flags) of the release or the bounds-checking build."""
+    if debug:
+        return LIB_DEBUG, BUILD_DIR + "_debug", ["-DLCE_DEBUG"]
+    return LIB, BUILD_DIR, []
+
+
+def up_to_date(debug: bool = False) -> bool:
+    lib = _variant(debug)[0]
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    if not force and not extra_flags and up_to_date():
-        return LIB
-    nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    flags = NVCC_FLAGS + (extra_flags or [])
+def _compile(nvcc: str, src: str, obj_dir: str, flags: list[str], verbose: bool) -> str:
+    obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if verbose or r.returncode:
+        sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
+    if r.returncode:
+        raise RuntimeError(f"nvcc failed on {os.path.basename(src)}")
+    return obj
 
-    def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if verbose or r.returncode:
-            sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
-        if r.returncode:
-            raise RuntimeError(f"nvcc failed on {os.path.basename(src)}")
-        return obj
 
-    srcs = sources()
-    with ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+def _link(nvcc: str, lib: str, objs: list[str]) -> None:
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode:
         sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
-        raise RuntimeError("link of liblce.so failed")
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"link of {os.path.basename(lib)} failed")
+    os.replace(tmp, lib)
+
+
+def build(force: bool = False, verbose: bool = False, debug: bool = False, both: bool = False) -> str:
+    """Builds the release library (or, with debug, the bounds-checking one;
+    with both, the two together in one pool of compiler processes) unless it
+    is newer than every source.  Returns the path of the (release) library."""
+    variants = [False, True] if both else [debug]
+    todo = [v for v in variants if force or not up_to_date(v)]
+    if todo:
+        nvcc = _nvcc()
+        jobs = []
+        for v in todo:
+            lib, obj_dir, extra = _variant(v)
+            os.makedirs(obj_dir, exist_ok=True)
+            jobs += [(v, src, obj_dir, NVCC_FLAGS + extra) for src in sources()]
+        with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+            objs = list(ex.map(lambda j: (j[0], _compile(nvcc, j[1], j[2], j[3], verbose)), jobs))
+        for v in todo:
+            _link(nvcc, _variant(v)[0], [o for w, o in objs if w == v])
+    return _variant(debug and not both)[0]
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv,
+                both="--both" in sys.argv))

@@ -355,6 +355,15 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     uint16_t* G2 = p.overlap ? reinterpret_cast<uint16_t*>(wsb + p.off_g2) : nullptr;
     float* pm2 = p.overlap ? reinterpret_cast<float*>(wsb + p.off_pm2) : nullptr;
 
+    // every GEMM launch of the call: the extents the bounds-checking build checks against
+    auto call_args = [&]() {
+        GemmArgs g = base_args(hdr);
+        g.cap_rows = p.C;
+        g.cap_pt = static_cast<int32_t>(2 * p.n_vt);
+        g.cap_gb = p.mt_chunk * 4;
+        return g;
+    };
+
     // operand maps of the whole X and W
     CUtensorMap mX_k, mW_k, mW16_mn;
     if (!map_16bit_2d(&mX_k, pb.X, pb.N, pb.H, pb.H, 64, BM) || !map_16bit_2d(&mW_k, pb.W, pb.V, pb.H, pb.H, 64, B_BOX_ROWS))
@@ -387,7 +396,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
         const int64_t r0 = c * p.C;
         const int64_t rows = (pb.N - r0) < p.C ? (pb.N - r0) : p.C;
         const int64_t mtf = cdiv(rows, form.rows);  // tiles of the GEMM form
-        GemmArgs a = base_args(hdr);
+        GemmArgs a = call_args();
         a.m_tiles = static_cast<int32_t>(mtf);
         a.n_tiles = static_cast<int32_t>(p.n_vt);
         a.k_blocks = static_cast<int32_t>(cdiv(pb.H, BK));
@@ -419,7 +428,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
         }
         LCE_LAUNCH(PK_LSE, launch_gemm(MODE_LSE, mX_k, mW_k, mW_k, a, grid_of(form, mtf * p.n_vt), s, form.pair));
         LCE_LAUNCH(PK_OTHER, launch_combine(pmc, ps, 2 * p.n_vt, p.C, rows, zt, pb.y + r0, pb.ignore_index, pb.V,
-                                            o.lse + r0, row_loss + r0, tcoef ? tcoef + r0 : nullptr, s));
+                                            o.lse + r0, row_loss + r0, tcoef ? tcoef + r0 : nullptr, &hdr->status,
+                                            s));
         return LCE_OK;
     };
     // The backward of chunk c; `rescaled`: its E was already turned into P.
@@ -433,9 +443,9 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
         if (do_fwd) {  // P = E 2^(tile max - lse), in place (unless the next forward did it)
             if (!rescaled)
                 LCE_LAUNCH(PK_OTHER, launch_p_rescale(Gc, p.ldg, rows, pb.V, pmc, p.C, o.lse + r0, crow + r0,
-                                                      nvc + c, gb, s));
+                                                      nvc + c, gb, &hdr->status, s));
         } else {   // recompute the logits; P = softmax (fp16)
-            GemmArgs a = base_args(hdr);
+            GemmArgs a = call_args();
             a.m_tiles = static_cast<int32_t>(mtf);
             a.n_tiles = static_cast<int32_t>(p.n_vt);
             a.k_blocks = static_cast<int32_t>(cdiv(pb.H, BK));
@@ -457,18 +467,18 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             LCE_LAUNCH(PK_P, launch_gemm(MODE_G, mX_k, mW_k, mW_k, a, grid_of(form, mtf * p.n_vt), s, form.pair));
             // c_i = -(sum of the row's non-target P), in a fixed order
             LCE_LAUNCH(PK_OTHER, launch_combine(nullptr, ps, 2 * p.n_vt, p.C, rows, nullptr, pb.y + r0,
-                                                pb.ignore_index, pb.V, nullptr, nullptr, tcoef + r0, s));
+                                                pb.ignore_index, pb.V, nullptr, nullptr, tcoef + r0, &hdr->status, s));
         }
         // P and X_c maps bounded to this chunk's rows: rows past it read as zero
         LCE_LAUNCH(PK_OTHER, launch_gather_f16(pb.X + r0 * pb.H, pb.H, crow + r0, nvc + c, rows, &hdr->amax_x_bits,
-                                               X16, do_fwd ? nullptr : Gc, p.ldg, s));
+                                               X16, do_fwd ? nullptr : Gc, p.ldg, &hdr->status, s));
         CUtensorMap mG_k, mG_mn, mX16_mn;
         if (!map_16bit_2d(&mG_k, Gc, rows, pb.V, p.ldg, 64, BM, true) ||
             !map_16bit_2d(&mG_mn, Gc, rows, pb.V, p.ldg, 64, 64, true) ||
             !map_16bit_2d(&mX16_mn, X16, rows, pb.H, pb.H, 64, 64, true))
             return LCE_ERR_CUDA;
         if (o.grad_X) {   // grad_X_c = s (P W - W[y])
-            GemmArgs a = base_args(hdr);
+            GemmArgs a = call_args();
             a.m_tiles = static_cast<int32_t>(mtf);
             a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
             a.k_blocks = static_cast<int32_t>(cdiv(pb.V, BK));
@@ -505,7 +515,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
                                                                pb.W, tcoef + r0, hdr, o.grad_X + r0 * pb.H, s));
         }
         {   // grad_W_acc (+)= s P^T X_c
-            GemmArgs a = base_args(hdr);
+            GemmArgs a = call_args();
             a.m_tiles = static_cast<int32_t>(cdiv(pb.V, form.rows));
             a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
             a.k_blocks = static_cast<int32_t>(cdiv(rows, BK));
@@ -532,8 +542,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             if (rows - k * LABEL_BLOCK <= 0) break;
             const int64_t blk = c * p.label_blocks_per_chunk + k;
             LCE_LAUNCH(PK_OTHER, launch_onehot_scatter(keys + blk * LABEL_BLOCK, runs + blk * LABEL_BLOCK,
-                                                       nrun + blk, pb.X + r0 * pb.H, tcoef + r0, pb.H, hdr,
-                                                       o.grad_W_acc, o.grad_W, lcsum, last && o.grad_W != nullptr,
+                                                       nrun + blk, pb.X + r0 * pb.H, tcoef + r0, pb.H, rows, pb.V,
+                                                       hdr, o.grad_W_acc, o.grad_W, lcsum, last && o.grad_W != nullptr,
                                                        4 * sm_count(), s));
         }
         // grad_b (after the scatter: the last chunk adds the target entries' sums per label)
@@ -708,6 +718,7 @@ lce_status_t lce_check_status(const void* ws, lce_stream_t stream) {
     if (cudaMemcpy(&st, ws, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return LCE_ERR_CUDA;
     if (st & STATUS_TIMEOUT) return LCE_ERR_TIMEOUT;
     if (st & STATUS_LABEL) return LCE_ERR_LABEL_RANGE;
+    if (st & STATUS_BOUNDS) return LCE_ERR_BOUNDS;
     return LCE_OK;
 }
 
@@ -720,6 +731,7 @@ const char* lce_status_string(lce_status_t status) {
         case LCE_ERR_LABEL_RANGE: return "label out of range";
         case LCE_ERR_TIMEOUT: return "device wait timed out";
         case LCE_ERR_CUDA: return "CUDA error";
+        case LCE_ERR_BOUNDS: return "index outside its buffer (bounds-checking build)";
         default: return "unknown status";
     }
 }

@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       int64_t n_pt, int64_t ldp, int64_t rows,
                                                       const float* __restrict__ zt, const int64_t* __restrict__ y,
                                                       int64_t ignore_index, int64_t V, float* __restrict__ lse,
-                                                      float* __restrict__ row_loss, float* __restrict__ tcoef) {
+                                                      float* __restrict__ row_loss, float* __restrict__ tcoef,
+                                                      unsigned* status) {
     __shared__ float wm[8][8], wsum[8][8];  // [warp][row of the block]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int part = warp * 4 + (lane >> 3);
@@ -102,7 +103,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     const int64_t per = (n_pt + 31) / 32;
     const int64_t t0 = part * per < n_pt ? part * per : n_pt, t1 = t0 + per < n_pt ? t0 + per : n_pt;
     float M = -INFINITY, S = 0.f;
-    if (ok) {
+    if (ok && LCE_IN(r < ldp && t1 <= n_pt, status)) {
         int64_t t = t0;
         for (; t + 8 <= t1; t += 8) {
             float m8[8], s8[8];
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(256) p_rescale_kernel(uint16_t* __restrict__ P
                                                         const float* __restrict__ lse,
                                                         const int* __restrict__ crow,
                                                         const int* __restrict__ n_valid,
-                                                        float* __restrict__ gb_part) {
+                                                        float* __restrict__ gb_part, unsigned* status) {
     __shared__ float colsum[8][256 + 4];
     constexpr float LOG2E = 1.4426950408889634f;
     const int cg = threadIdx.x & 31, rr = threadIdx.x >> 5;
@@ -185,6 +186,7 @@ __global__ void __launch_bounds__(256) p_rescale_kernel(uint16_t* __restrict__ P
             continue;
         }
         const int64_t r = crow[j];  // chunk row
+        if (!LCE_IN(r >= 0 && r < ldp, status)) continue;
         // the forward kept one max per 128-column half tile
         const float f = exp2f(pm[(2 * tile + (cg >> 4)) * ldp + r] - lse[r] * LOG2E);
         const uint4 w = *ptr;
@@ -274,7 +276,8 @@ __global__ void zero_ignored_rows_kernel(const int* __restrict__ dmap, int64_t N
 // P_tail, the same tail rows of P are zeroed too.
 __global__ void gather_f16_kernel(const uint16_t* __restrict__ X_chunk, int64_t H, const int* __restrict__ crow,
                                   const int* __restrict__ n_valid, int64_t max_rows, const unsigned* amax_bits,
-                                  uint16_t* __restrict__ X16, uint16_t* __restrict__ P_tail, int64_t ldg) {
+                                  uint16_t* __restrict__ X16, uint16_t* __restrict__ P_tail, int64_t ldg,
+                                  unsigned* status) {
     const float f = ldexpf(1.f, operand_scale_exp(*amax_bits));
     const int64_t nv = *n_valid;
     int64_t end = (nv + 63) / 64 * 64;
@@ -284,7 +287,7 @@ __global__ void gather_f16_kernel(const uint16_t* __restrict__ X_chunk, int64_t 
     for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < end * h8; e += stride) {
         const int64_t j = e / h8, k = e - j * h8;
         uint4 o = make_uint4(0u, 0u, 0u, 0u);
-        if (j < nv) {
+        if (j < nv && LCE_IN(crow[j] >= 0 && crow[j] < max_rows, status)) {
             const uint4 w = reinterpret_cast<const uint4*>(X_chunk + static_cast<int64_t>(crow[j]) * H)[k];
             const uint32_t u[4] = {w.x, w.y, w.z, w.w};
             uint32_t r[4];
@@ -450,8 +453,8 @@ __global__ void __launch_bounds__(256) onehot_scatter_kernel(const unsigned long
                                                              const unsigned long long* __restrict__ runs,
                                                              const int* __restrict__ run_count,
                                                              const uint16_t* __restrict__ X_chunk,
-                                                             const float* __restrict__ tcoef, int64_t H,
-                                                             const WsHeader* hdr, float* grad_W_acc,
+                                                             const float* __restrict__ tcoef, int64_t H, int64_t rows,
+                                                             int64_t V, WsHeader* hdr, float* grad_W_acc,
                                                              uint16_t* grad_W, float* label_csum, int write_bf16) {
     __shared__ float part[3][64][9];
     const int ct = threadIdx.x & 63, rg = threadIdx.x >> 6;
@@ -460,10 +463,11 @@ __global__ void __launch_bounds__(256) onehot_scatter_kernel(const unsigned long
     const float s = hdr->scale;
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
         const unsigned long long run = runs[item / slabs];
-        const int64_t start = static_cast<int64_t>(run & 0xFFFFFFFFull), end = static_cast<int64_t>(run >> 32);
-        const unsigned long long v = keys[start] >> 32;
+        int64_t start = static_cast<int64_t>(run & 0xFFFFFFFFull), end = static_cast<int64_t>(run >> 32);
+        if (!LCE_IN(start < end && end <= LABEL_BLOCK && item / slabs < LABEL_BLOCK, &hdr->status)) start = end = 0;
+        const unsigned long long v = end > start ? keys[start] >> 32 : 0;
         const int64_t h = static_cast<int64_t>(item % slabs) * 512 + ct * 8;
-        const bool active = h < H;
+        const bool active = h < H && end > start && LCE_IN(v < static_cast<unsigned long long>(V), &hdr->status);
         float sum[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) sum[k] = 0.f;
@@ -474,7 +478,8 @@ __global__ void __launch_bounds__(256) onehot_scatter_kernel(const unsigned long
                 float c[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int64_t row = static_cast<int64_t>(keys[j + 4 * u] & 0xFFFFFFFFull);
+                    int64_t row = static_cast<int64_t>(keys[j + 4 * u] & 0xFFFFFFFFull);
+                    if (!LCE_IN(row < rows, &hdr->status)) row = 0;
                     w[u] = *reinterpret_cast<const uint4*>(X_chunk + row * H + h);
                     c[u] = tcoef[row];
                 }
@@ -482,7 +487,8 @@ __global__ void __launch_bounds__(256) onehot_scatter_kernel(const unsigned long
                 for (int u = 0; u < 4; ++u) fma_bf16x8(sum, c[u], w[u]);
             }
             for (; j < end; j += 4) {
-                const int64_t row = static_cast<int64_t>(keys[j] & 0xFFFFFFFFull);
+                int64_t row = static_cast<int64_t>(keys[j] & 0xFFFFFFFFull);
+                if (!LCE_IN(row < rows, &hdr->status)) row = 0;
                 fma_bf16x8(sum, tcoef[row], *reinterpret_cast<const uint4*>(X_chunk + row * H + h));
             }
         }
@@ -520,11 +526,14 @@ __global__ void __launch_bounds__(256) onehot_scatter_kernel(const unsigned long
         }
         if (label_csum && item % slabs == 0 && threadIdx.x < 32) {
             float c = 0.f;
-            for (int64_t jj = start + threadIdx.x; jj < end; jj += 32)
-                c += tcoef[static_cast<int64_t>(keys[jj] & 0xFFFFFFFFull)];
+            for (int64_t jj = start + threadIdx.x; jj < end; jj += 32) {
+                const int64_t row = static_cast<int64_t>(keys[jj] & 0xFFFFFFFFull);
+                if (LCE_IN(row < rows, &hdr->status)) c += tcoef[row];
+            }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
-            if (threadIdx.x == 0) label_csum[v] += c;
+            if (threadIdx.x == 0 && end > start && LCE_IN(v < static_cast<unsigned long long>(V), &hdr->status))
+                label_csum[v] += c;
         }
         __syncthreads();
     }
@@ -575,7 +584,8 @@ __global__ void gradx_split_reduce_kernel(const float* __restrict__ split_out, i
                                           int64_t H, const int* __restrict__ crow, const int* __restrict__ n_valid,
                                           const int64_t* __restrict__ y, int64_t ignore_index, int64_t V,
                                           const uint16_t* __restrict__ W, const float* __restrict__ tcoef,
-                                          const WsHeader* hdr, uint16_t* __restrict__ grad_X_chunk) {
+                                          const WsHeader* hdr, uint16_t* __restrict__ grad_X_chunk,
+                                          int64_t max_rows) {
     const float s = hdr->scale;
     const float f = ldexpf(s, -(P_SCALE_EXP + operand_scale_exp(hdr->amax_w_bits)));
     const int64_t nv = *n_valid, h8 = H / 8;
@@ -593,6 +603,7 @@ __global__ void gradx_split_reduce_kernel(const float* __restrict__ split_out, i
             sum[4] += b.x; sum[5] += b.y; sum[6] += b.z; sum[7] += b.w;
         }
         const int64_t r = crow[j];
+        if (!LCE_IN(r >= 0 && r < max_rows, const_cast<unsigned*>(&hdr->status))) continue;
         const int64_t yr = y[r];
         float w[8];
         const bool valid = yr != ignore_index && yr >= 0 && yr < V;
@@ -718,11 +729,11 @@ cudaError_t launch_label_sort(const int64_t* y, int64_t N, int64_t C, int64_t bl
 }
 
 cudaError_t launch_onehot_scatter(const unsigned long long* keys, const unsigned long long* runs, const int* run_count,
-                                  const uint16_t* X_chunk, const float* tcoef, int64_t H, const WsHeader* hdr,
-                                  float* grad_W_acc, uint16_t* grad_W, float* label_csum, int write_bf16, int grid,
-                                  cudaStream_t s) {
-    onehot_scatter_kernel<<<grid, 256, 0, s>>>(keys, runs, run_count, X_chunk, tcoef, H, hdr, grad_W_acc, grad_W,
-                                               label_csum, write_bf16);
+                                  const uint16_t* X_chunk, const float* tcoef, int64_t H, int64_t rows, int64_t V,
+                                  WsHeader* hdr, float* grad_W_acc, uint16_t* grad_W, float* label_csum,
+                                  int write_bf16, int grid, cudaStream_t s) {
+    onehot_scatter_kernel<<<grid, 256, 0, s>>>(keys, runs, run_count, X_chunk, tcoef, H, rows, V, hdr, grad_W_acc,
+                                               grad_W, label_csum, write_bf16);
     return cudaGetLastError();
 }
 
@@ -734,11 +745,11 @@ cudaError_t launch_scale(WsHeader* hdr, float grad_scale, const float* d_grad_ou
 
 cudaError_t launch_combine(const float* part_m, const float* part_s, int64_t n_pt, int64_t ldp, int64_t rows,
                            const float* zt, const int64_t* y, int64_t ignore_index, int64_t V, float* lse,
-                           float* row_loss, float* tcoef, cudaStream_t s) {
+                           float* row_loss, float* tcoef, unsigned* status, cudaStream_t s) {
     const int threads = 256;  // 8 rows, 32 threads each
     const int64_t blocks = (rows + 7) / 8;
     combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(part_m, part_s, n_pt, ldp, rows, zt, y,
-                                                                      ignore_index, V, lse, row_loss, tcoef);
+                                                                      ignore_index, V, lse, row_loss, tcoef, status);
     return cudaGetLastError();
 }
 
@@ -782,11 +793,11 @@ cudaError_t launch_to_f16_scaled(const uint16_t* x, int64_t n, const unsigned* a
 
 cudaError_t launch_p_rescale(uint16_t* P, int64_t ldg, int64_t rows, int64_t V, const float* pm, int64_t ldp,
                              const float* lse, const int* crow, const int* n_valid, float* gb_part,
-                             cudaStream_t s) {
+                             unsigned* status, cudaStream_t s) {
     // every 32-row block of every 128-row tile writes its column sums (zeros
     // past the last row), the layout the grad_b accumulation reads
     const dim3 grid(static_cast<unsigned>((rows + 127) / 128 * 4), static_cast<unsigned>((V + 255) / 256));
-    p_rescale_kernel<<<grid, 256, 0, s>>>(P, ldg, rows, V, pm, ldp, lse, crow, n_valid, gb_part);
+    p_rescale_kernel<<<grid, 256, 0, s>>>(P, ldg, rows, V, pm, ldp, lse, crow, n_valid, gb_part, status);
     return cudaGetLastError();
 }
 
@@ -805,10 +816,11 @@ cudaError_t launch_zero_ignored_rows(const int* dmap, int64_t N, int64_t H, uint
 
 cudaError_t launch_gather_f16(const uint16_t* X_chunk, int64_t H, const int* crow, const int* n_valid,
                               int64_t max_rows, const unsigned* amax_bits, uint16_t* X16, uint16_t* P_tail,
-                              int64_t ldg, cudaStream_t s) {
+                              int64_t ldg, unsigned* status, cudaStream_t s) {
     const int64_t want = (max_rows * (H / 8) + 255) / 256;
     const int blocks = static_cast<int>(want < 1 ? 1 : (want < 4096 ? want : 4096));
-    gather_f16_kernel<<<blocks, 256, 0, s>>>(X_chunk, H, crow, n_valid, max_rows, amax_bits, X16, P_tail, ldg);
+    gather_f16_kernel<<<blocks, 256, 0, s>>>(X_chunk, H, crow, n_valid, max_rows, amax_bits, X16, P_tail, ldg,
+                                             status);
     return cudaGetLastError();
 }
 
@@ -833,7 +845,7 @@ cudaError_t launch_gradx_split_reduce(const float* split_out, int64_t splits, in
     const int64_t want = (max_rows * (H / 8) + 255) / 256;
     const int blocks = static_cast<int>(want < 1 ? 1 : (want < 4096 ? want : 4096));
     gradx_split_reduce_kernel<<<blocks, 256, 0, s>>>(split_out, splits, split_stride, H, crow, n_valid, y,
-                                                     ignore_index, V, W, tcoef, hdr, grad_X_chunk);
+                                                     ignore_index, V, W, tcoef, hdr, grad_X_chunk, max_rows);
     return cudaGetLastError();
 }
 

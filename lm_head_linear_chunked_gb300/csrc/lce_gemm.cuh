@@ -248,7 +248,7 @@ __device__ __forceinline__ void side_unit(const GemmArgs& a, const SideJob& j, i
     float fl = 0.f;
     {
         const int64_t r8 = rb * 8 + (lane & 7);
-        if (lane < 16 && r8 < j.nv) {
+        if (lane < 16 && r8 < j.nv && LCE_IN(a.side_crow[r8] >= 0 && a.side_crow[r8] < a.side_rows, a.status)) {
             const int64_t r = a.side_crow[r8];  // chunk row
             const float* pm = a.side_pm + (2 * tile + (lane >> 3)) * a.ldp;
             fl = exp2f(pm[r] - a.side_lse[r] * LOG2E_F);
@@ -378,12 +378,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
                     v[i] = e * P_SCALE;
                 }
             }
-            if (a.g && prow >= 0) store_f16_32(a.g + prow * a.ldg + c0, v, static_cast<int>(min64(32, a.ldg - c0)));
+            if (a.g && prow >= 0 && LCE_IN(prow < a.cap_rows, a.status))
+                store_f16_32(a.g + prow * a.ldg + c0, v, static_cast<int>(min64(32, a.ldg - c0)));
         }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) release_acc<PAIR>(empty_bar);
-        if (row_ok) {
+        if (row_ok && LCE_IN(2 * n + half < a.cap_pt && row < a.ldp && row < a.cap_rows, a.status)) {
             // one partial per 128-column half tile
             a.part_m[(2 * static_cast<int64_t>(n) + half) * a.ldp + row] = mx;
             a.part_s[(2 * static_cast<int64_t>(n) + half) * a.ldp + row] = sm;
@@ -412,7 +413,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
                 v[i] = (valid && i < nv && i != kk) ? p : 0.f;
                 se += v[i];
             }
-            if (prow >= 0) {
+            if (prow >= 0 && LCE_IN(prow < a.cap_rows, a.status)) {
                 float ps[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) ps[i] = v[i] * P_SCALE;
@@ -420,13 +421,15 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
             }
             if (a.gb_part && static_cast<int64_t>(m) * BM < a.M) {  // (a pair's second tile may lie past M)
                 const float cs = warp_column_sums(v, lane);
-                if (c0 + lane < a.N) a.gb_part[(static_cast<int64_t>(m) * 4 + q) * a.N + c0 + lane] = cs;
+                if (c0 + lane < a.N && LCE_IN(static_cast<int64_t>(m) * 4 + q < a.cap_gb, a.status))
+                    a.gb_part[(static_cast<int64_t>(m) * 4 + q) * a.N + c0 + lane] = cs;
             }
         }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) release_acc<PAIR>(empty_bar);
-        if (row_ok && a.part_s) a.part_s[(2 * static_cast<int64_t>(n) + half) * a.ldp + row] = se;
+        if (row_ok && a.part_s && LCE_IN(2 * n + half < a.cap_pt && row < a.ldp, a.status))
+            a.part_s[(2 * static_cast<int64_t>(n) + half) * a.ldp + row] = se;
     } else if constexpr (MODE == MODE_GRADX) {
       if (a.k_splits > 1) {
         // one K slice of a split product: the raw fp32 partial sums, finished
@@ -442,7 +445,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = 0.f;
             }
-            if (row_ok) store_f32_32(dst + row * a.N + c0, v, static_cast<int>(min64(32, a.N - c0)));
+            if (row_ok && LCE_IN(ks < a.k_splits && row < a.cap_rows, a.status))
+                store_f32_32(dst + row * a.N + c0, v, static_cast<int>(min64(32, a.N - c0)));
         }
         tc_fence_before_sync();
         __syncwarp();
@@ -452,9 +456,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         // entry, c_i = p_{i,y_i} - 1; P rows of ignored rows are 0
         const float s = *a.scale;
         const float f = ldexpf(s, -(P_SCALE_EXP + operand_scale_exp(*a.b_amax_bits)));
-        const int64_t orow = (a.row_map && row_ok) ? static_cast<int64_t>(a.row_map[row]) : row;  // chunk row
+        int64_t orow = (a.row_map && row_ok) ? static_cast<int64_t>(a.row_map[row]) : row;  // chunk row
+        const bool orow_ok = !row_ok || LCE_IN(orow >= 0 && orow < a.cap_rows, a.status);
+        if (!orow_ok) orow = 0;
         const int64_t yr = row_ok ? a.y[orow] : a.ignore_index;
-        const bool valid = row_ok && yr != a.ignore_index && yr >= 0 && yr < a.V;
+        const bool valid = row_ok && orow_ok && yr != a.ignore_index && yr >= 0 && yr < a.V;
         const float sc = valid ? s * a.tcoef[orow] : 0.f;
         const uint16_t* wy = a.w_rows + (valid ? yr : 0) * a.ldw;
 #pragma unroll 1
@@ -475,7 +481,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= f;
                 }
-                store_bf16_32(a.out_bf16 + orow * a.ld_out + c0, v, static_cast<int>(min64(32, a.N - c0)));
+                if (orow_ok) store_bf16_32(a.out_bf16 + orow * a.ld_out + c0, v, static_cast<int>(min64(32, a.N - c0)));
             }
         }
         tc_fence_before_sync();
@@ -512,7 +518,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
                                  : make_float4(s * v[4 * k], s * v[4 * k + 1], s * v[4 * k + 2], s * v[4 * k + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0 && row_base < m_rows) {
+                if (lane == 0 && row_base < m_rows && LCE_IN((c0 & 3) == 0 && c0 < a.N && row_base >= 0, a.status)) {
                     if (a.acc_first)
                         tma_store_2d(map_c, sbuf, static_cast<int32_t>(c0), static_cast<int32_t>(row_base));
                     else
@@ -675,6 +681,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     const uint32_t sa = base + stage * STAGE_BYTES;
                     const uint32_t sb = sa + A_STAGE_BYTES;
                     const int32_t k0 = kb * BK;
+                    // innermost coordinates: multiples of 8 16-bit elements (16 bytes)
+                    (void)LCE_IN((k0 & 7) == 0 && ((m * BM) & 7) == 0 && ((n * BN) & 7) == 0, args.status);
                     if constexpr (!T::A_MN) {
                         tma_load_2d(sa, &map_a, fb, k0, args.a_y0 + m * BM);
                     } else {

@@ -145,6 +145,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     const uint32_t sa = base + stage * PAIR_STAGE_BYTES;
                     const uint32_t sb = sa + A_STAGE_BYTES;
                     const int32_t k0 = kb * BK;
+                    // innermost coordinates: multiples of 8 16-bit elements (16 bytes)
+                    (void)LCE_IN((k0 & 7) == 0 && (arow & 7) == 0 && (bcol & 7) == 0, args.status);
                     if constexpr (!T::A_MN) {
                         tma_load_2d_pair(sa, &map_a, fb, k0, args.a_y0 + arow);
                     } else {

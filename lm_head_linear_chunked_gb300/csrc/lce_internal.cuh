@@ -78,6 +78,21 @@ static_assert(GEMM_SMEM_BYTES + EPI_STAGE_BYTES <= 232448 && GEMM_PAIR_SMEM_BYTE
 // Device status word bits (bit k set = lce_status_t k was raised).
 constexpr unsigned STATUS_LABEL = 1u << LCE_ERR_LABEL_RANGE;
 constexpr unsigned STATUS_TIMEOUT = 1u << LCE_ERR_TIMEOUT;
+constexpr unsigned STATUS_BOUNDS = 1u << LCE_ERR_BOUNDS;
+
+// Bounds-checking build (LCE_DEBUG): LCE_IN(cond, status) is `cond`, and a
+// false condition also raises STATUS_BOUNDS in the call's status word; the
+// caller skips the access it guards.  In the release build it is `true` and
+// `cond` is not evaluated.
+#ifdef LCE_DEBUG
+__device__ __forceinline__ bool dbg_in(bool ok, unsigned* status) {
+    if (!ok) atomicOr(status, STATUS_BOUNDS);
+    return ok;
+}
+#define LCE_IN(cond, status) (::lce::dbg_in((cond), (status)))
+#else
+#define LCE_IN(cond, status) (true)
+#endif
 
 // The gradient GEMMs take fp16 operands (11 significant bits, against bf16's
 // 8): P is stored as fp16(p * 2^P_SCALE_EXP), and W and X are converted to
@@ -187,6 +202,12 @@ struct GemmArgs {
     int64_t side_rows;         // its number of chunk rows
     unsigned* status;
     uint64_t timeout_ns;
+    // Extents the bounds-checking build checks against: rows of the buffers
+    // indexed by chunk row (target logits, partial columns, E/P rows, split
+    // partial rows, c_i), partial rows (2 x vocabulary tiles), grad_b partial rows.
+    int64_t cap_rows;
+    int32_t cap_pt;
+    int64_t cap_gb;
 };
 
 // Launches the GEMM kernel of `mode`: with `pair`, the pair form (grid =
@@ -218,7 +239,7 @@ cudaError_t launch_label_sort(const int64_t* y, int64_t N, int64_t C, int64_t bl
 // label_csum[v] += sum of those c_i (for grad_b).
 cudaError_t launch_onehot_scatter(const unsigned long long* keys, const unsigned long long* runs,
                                   const int* run_count, const uint16_t* X_chunk, const float* tcoef, int64_t H,
-                                  const WsHeader* hdr, float* grad_W_acc, uint16_t* grad_W,
+                                  int64_t rows, int64_t V, WsHeader* hdr, float* grad_W_acc, uint16_t* grad_W,
                                   float* label_csum, int write_bf16, int grid, cudaStream_t s);
 // s = grad_scale * grad_output / n_valid (mean), or grad_scale * grad_output (sum_reduction).
 cudaError_t launch_scale(WsHeader* hdr, float grad_scale, const float* d_grad_output,
@@ -229,7 +250,7 @@ cudaError_t launch_scale(WsHeader* hdr, float grad_scale, const float* d_grad_ou
 // the non-target P (the recompute path) and only tcoef = -sum is written.
 cudaError_t launch_combine(const float* part_m, const float* part_s, int64_t n_vt, int64_t ldp,
                            int64_t rows, const float* zt, const int64_t* y, int64_t ignore_index, int64_t V,
-                           float* lse, float* row_loss, float* tcoef, cudaStream_t s);
+                           float* lse, float* row_loss, float* tcoef, unsigned* status, cudaStream_t s);
 // loss = mean (or, with sum_reduction, sum) of the row losses of the valid rows.
 cudaError_t launch_loss(const float* row_loss, int64_t N, const WsHeader* hdr, float* loss,
                         int64_t* n_valid_out, bool sum_reduction, cudaStream_t s);
@@ -239,7 +260,7 @@ cudaError_t launch_grad_b(const float* gb_part, int64_t parts, int64_t V, const 
 cudaError_t launch_wait_probe(unsigned* status, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_p_rescale(uint16_t* P, int64_t ldg, int64_t rows, int64_t V, const float* pm, int64_t ldp,
                              const float* lse, const int* crow, const int* n_valid, float* gb_part,
-                             cudaStream_t s);
+                             unsigned* status, cudaStream_t s);
 cudaError_t launch_scale_grads(int64_t N, int64_t H, int64_t V, const float* d_grad_output, uint16_t* grad_X,
                                const float* grad_W_acc, uint16_t* grad_W, const float* grad_b_acc,
                                uint16_t* grad_b, cudaStream_t s);
@@ -248,7 +269,7 @@ cudaError_t launch_compact_rows(const int64_t* y, int64_t N, int64_t C, int64_t 
 cudaError_t launch_zero_ignored_rows(const int* dmap, int64_t N, int64_t H, uint16_t* grad_X, cudaStream_t s);
 cudaError_t launch_gather_f16(const uint16_t* X_chunk, int64_t H, const int* crow, const int* n_valid,
                               int64_t max_rows, const unsigned* amax_bits, uint16_t* X16, uint16_t* P_tail,
-                              int64_t ldg, cudaStream_t s);
+                              int64_t ldg, unsigned* status, cudaStream_t s);
 cudaError_t launch_gradx_split_reduce(const float* split_out, int64_t splits, int64_t split_stride, int64_t H,
                                       const int* crow, const int* n_valid, int64_t max_rows, const int64_t* y,
                                       int64_t ignore_index, int64_t V, const uint16_t* W, const float* tcoef,
