@@ -4,7 +4,7 @@ a 8192-wide hidden state, and chunks of one row next to chunks of all rows."""
 import pytest
 
 import lm_head_linear_chunked_gb300 as lce
-from tests.gpu_util import check_against_oracle, fp16_acc_bound
+from tests.gpu_util import check_against_oracle
 from tests.test_gpu_parity import oracle_of, random_problem, run_fused
 
 pytestmark = pytest.mark.gpu
@@ -22,5 +22,4 @@ def test_extreme_shape(N, H, V, bias, chunk):
     out = run_fused(X, W, b, y, chunk)
     assert out["status"] == 0
     ref = oracle_of(X, W, b, y)
-    check_against_oracle(out, ref, has_bias=bias,
-                         acc_bound=fp16_acc_bound(X, W, b, y, ref["lse"], 1.0 / max(ref["n_valid"], 1)))
+    check_against_oracle(out, ref, has_bias=bias)

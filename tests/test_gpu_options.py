@@ -2,12 +2,11 @@
 oracle: reduction "sum" (loss = sum over valid rows, gradient scale without
 the division by n_valid) and accumulation of the FP32 gradient accumulators
 across calls (gradient accumulation over micro-batches)."""
-import numpy as np
 import pytest
 
 import lm_head_linear_chunked_gb300 as lce
 import oracle
-from tests.gpu_util import F32_ACC_TOL, assert_grad, check_against_oracle, dev_bf16, dev_i64, fp16_acc_bound
+from tests.gpu_util import F32_ACC_TOL, assert_grad, check_against_oracle, dev_bf16, dev_i64
 from tests.test_gpu_parity import random_problem
 
 pytestmark = pytest.mark.gpu
@@ -29,7 +28,7 @@ def test_sum_reduction_fused(N, H, V, bias, chunk):
     out = lce.fused(Xd, Wd, bd, yd, chunk_rows=chunk, grad_scale=0.5, reduction="sum")
     _ok(out)
     ref = oracle.fused(X, W, b, y, grad_scale=0.5, reduction="sum")
-    check_against_oracle(out, ref, has_bias=bias, acc_bound=fp16_acc_bound(X, W, b, y, ref["lse"], 0.5))
+    check_against_oracle(out, ref, has_bias=bias)
 
 
 def test_sum_reduction_forward_and_backward():
@@ -41,7 +40,7 @@ def test_sum_reduction_forward_and_backward():
     check_against_oracle(f, ref, has_bias=True, bwd=False)
     g = lce.backward(Xd, Wd, bd, yd, f["lse"], chunk_rows=256, reduction="sum")
     _ok(g)
-    check_against_oracle(g, ref, has_bias=True, fwd=False, acc_bound=fp16_acc_bound(X, W, b, y, ref["lse"], 1.0))
+    check_against_oracle(g, ref, has_bias=True, fwd=False)
 
 
 @pytest.mark.parametrize("entry", ["fused", "backward"])
@@ -74,8 +73,7 @@ def test_accumulate_over_micro_batches(entry, reduction):
         acc_W, acc_b = out["grad_W_acc"], out["grad_b_acc"]
     ref = oracle.fused(X, W, b, y, reduction=reduction)
     s = 1.0 / n_all if reduction == "mean" else 1.0
-    bound = fp16_acc_bound(X, W, b, y, ref["lse"], s)
-    assert_grad(acc_W, ref["grad_W"], F32_ACC_TOL, "accumulated grad_W_acc", bound + 1e-5 * np.abs(ref["grad_W"]).max())
+    assert_grad(acc_W, ref["grad_W"], F32_ACC_TOL, "accumulated grad_W_acc")
     assert_grad(acc_b, ref["grad_b"], F32_ACC_TOL, "accumulated grad_b_acc")
     # the bf16 outputs of the last call are the cast of the totals
     assert torch.equal(out["grad_W"], acc_W.to(torch.bfloat16))

@@ -9,7 +9,7 @@ import lce_inputs as L
 import lm_head_linear_chunked_gb300 as lce
 import oracle
 from tests.gpu_util import (BF16_GRAD_TOL, F32_ACC_TOL, LSE_ATOL, assert_grad, check_against_oracle, dev_bf16,
-                            dev_i64, fp16_acc_bound, host_f64)
+                            dev_i64, host_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -145,11 +145,10 @@ def test_chunk_size_invariance():
 def test_ragged_shapes(N, H, V, bias):
     X, W, b, y = random_problem(N + H + V, N, H, V, bias=bias, ignore_frac=0.2)
     ref = oracle_of(X, W, b, y)
-    bound = fp16_acc_bound(X, W, b, y, ref["lse"], 1.0 / max(ref["n_valid"], 1))
     for chunk in (0, 100):
         out = run_fused(X, W, b, y, chunk)
         assert out["status"] == 0
-        check_against_oracle(out, ref, has_bias=bias, acc_bound=bound)
+        check_against_oracle(out, ref, has_bias=bias)
 
 
 # ---------------------------------------------------------------- scales and degenerate cases
@@ -159,8 +158,7 @@ def test_grad_scale_and_grad_output():
     out = run_fused(X, W, b, y, 64, grad_scale=0.5, grad_output=3.0)
     assert out["status"] == 0
     ref = oracle_of(X, W, b, y, grad_scale=0.5, grad_output=3.0)
-    bound = fp16_acc_bound(X, W, b, y, ref["lse"], 1.5 / ref["n_valid"])
-    check_against_oracle(out, ref, has_bias=True, acc_bound=bound)
+    check_against_oracle(out, ref, has_bias=True)
 
 
 def test_all_rows_ignored():
@@ -206,8 +204,7 @@ def test_large_logits_do_not_overflow():
     out = run_fused(X, W, None, y, 0)
     assert out["status"] == 0
     ref = oracle_of(X, W, None, y)
-    check_against_oracle(out, ref, has_bias=False,
-                         acc_bound=fp16_acc_bound(X, W, None, y, ref["lse"], 1.0 / ref["n_valid"]))
+    check_against_oracle(out, ref, has_bias=False)
 
 
 def test_custom_ignore_index():
@@ -217,8 +214,7 @@ def test_custom_ignore_index():
     out = run_fused(X, W, None, y, 0, ignore_index=-1)
     assert out["status"] == 0
     ref = oracle.fused(X, W, None, y, ignore_index=-1)
-    check_against_oracle(out, ref, has_bias=False,
-                         acc_bound=fp16_acc_bound(X, W, None, y, ref["lse"], 1.0 / ref["n_valid"], ignore_index=-1))
+    check_against_oracle(out, ref, has_bias=False)
 
 
 def test_label_out_of_range_sets_status():
@@ -245,11 +241,10 @@ def test_chunk_spanning_several_label_blocks():
     one-hot updates of the same grad_W rows must all land."""
     X, W, b, y = random_problem(13, 20000, 64, 512, bias=True)
     ref = oracle_of(X, W, b, y)
-    bound = fp16_acc_bound(X, W, b, y, ref["lse"], 1.0 / ref["n_valid"])
     for chunk in (20000, 9000):
         out = run_fused(X, W, b, y, chunk)
         assert out["status"] == 0
-        check_against_oracle(out, ref, has_bias=True, acc_bound=bound)
+        check_against_oracle(out, ref, has_bias=True)
 
 
 def test_overlapped_rescale_matches_oracle_and_recompute():
@@ -261,10 +256,9 @@ def test_overlapped_rescale_matches_oracle_and_recompute():
     import torch
     X, W, b, y = random_problem(91, 9000, 128, 4096, bias=False, ignore_frac=0.2)
     ref = oracle_of(X, W, b, y)
-    bound = fp16_acc_bound(X, W, b, y, ref["lse"], 1.0 / max(ref["n_valid"], 1))
     out = run_fused(X, W, b, y, 4096)
     assert out["status"] == 0
-    check_against_oracle(out, ref, has_bias=False, acc_bound=bound)
+    check_against_oracle(out, ref, has_bias=False)
     Xd, Wd, yd = dev_bf16(X), dev_bf16(W), dev_i64(y)
     f = lce.forward(Xd, Wd, None, yd, chunk_rows=4096)
     g = lce.backward(Xd, Wd, None, yd, f["lse"], chunk_rows=4096)

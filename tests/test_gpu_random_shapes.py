@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 import lm_head_linear_chunked_gb300 as lce
-from tests.gpu_util import check_against_oracle, fp16_acc_bound
+from tests.gpu_util import check_against_oracle
 from tests.test_gpu_parity import oracle_of, random_problem, run_fused
 
 pytestmark = pytest.mark.gpu
@@ -39,5 +39,4 @@ def test_random_shape(form, case):
         lce.lce_set_gemm_form(prev)
     assert out["status"] == 0
     ref = oracle_of(X, W, b, y)
-    check_against_oracle(out, ref, has_bias=bias,
-                         acc_bound=fp16_acc_bound(X, W, b, y, ref["lse"], 1.0 / max(ref["n_valid"], 1)))
+    check_against_oracle(out, ref, has_bias=bias)
