@@ -38,6 +38,29 @@ def test_library_exports_every_declared_symbol():
     assert set(declared_symbols()) <= set(lce._SIGS)
 
 
+def test_bounds_checking_library_has_the_same_entry_points():
+    """liblce_debug.so (the sources compiled with LCE_DEBUG) is built beside
+    liblce.so and exports the same declared entry points; its host-side
+    argument checks answer the same way."""
+    from lm_head_linear_chunked_gb300 import build
+    lib_path, obj_dir, flags = build._variant(True)
+    assert lib_path.endswith("liblce_debug.so") and "-DLCE_DEBUG" in flags and obj_dir != build.BUILD_DIR
+    assert os.path.exists(lib_path)
+    D = ctypes.CDLL(lib_path)
+    for n in declared_symbols():
+        assert hasattr(D, n), n
+    out = ctypes.c_size_t(0)
+    f = D.lce_workspace_size
+    f.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
+    assert f(4096, 1024, 32768, 256, 1, lce.WS_FUSED, ctypes.byref(out)) == 0
+    assert out.value == lce.lce_workspace_size(4096, 1024, 32768, 256, True, lce.WS_FUSED)
+    assert f(0, 1024, 32768, 256, 1, lce.WS_FUSED, ctypes.byref(out)) == 1  # LCE_ERR_INVALID_ARG
+    g = D.lce_status_string
+    g.restype = ctypes.c_char_p
+    g.argtypes = [ctypes.c_int]
+    assert b"bounds" in g(7)
+
+
 def test_status_strings():
     for code, name in lce.STATUS.items():
         assert lce.lce_status_string(code)
