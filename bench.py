@@ -264,7 +264,8 @@ class ClockSampler:
                 if val.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(pw) if pw else None, "samples": len(rows), "reasons": sorted(reasons)}
+                "power_w_max": max(pw) if pw else None, "power_w_mean": statistics.mean(pw) if pw else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------- our library
@@ -572,6 +573,9 @@ def run_ours(args, w):
         "workspace_bytes": nws,
         "logits_bytes_avoided": N * V * 2,
         "clocks": clocks,
+        # energy of one step from the power samples of the timed region (board power as nvidia-smi reports it);
+        # under the power cap, time per step follows energy per step
+        "joules_per_step": clocks["power_w_mean"] * t_step if clocks.get("power_w_mean") else None,
         "e2e": e2e,
         "separate_entry_points": split,
     }

@@ -1,5 +1,5 @@
 """The benchmark's clock record: the median SM clock under load, the maximum
-clock, the peak power and the throttle reasons active during the timed
+clock, the peak and mean power and the throttle reasons active during the timed
 region, read from nvidia-smi's CSV samples.  A fake nvidia-smi on PATH
 stands in for the tool, so this runs without a GPU."""
 import os
@@ -42,6 +42,7 @@ def test_summary_of_samples(monkeypatch, tmp_path):
     assert s["sm_mhz"] == 1450.0  # median of 1400, 1500, 1450; [N/A] is skipped
     assert s["sm_max_mhz"] == 2070.0
     assert s["power_w_max"] == 1398.5
+    assert abs(s["power_w_mean"] - (1398.5 + 1201.0 + 1300.25) / 3) < 1e-9  # the energy per step uses the mean
     assert s["reasons"] == ["sw_power_cap"]
 
 
