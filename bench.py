@@ -49,21 +49,20 @@ WORKLOAD = "qwen3-8b-head-N131072-H4096-V151936"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 # DRAM bytes (read + write) of one full-size launch of the dominant GEMM role
 # on this workload.  ncu multi-metric captures stay on small cases, so the
-# figure is scaled: the forward logits launch of a 16384-row chunk (keeping E
+# figure is scaled: the forward logits launch of an 8192-row chunk (keeping E
 # and rescaling the previous chunk's) was captured at V = 16384 and 32768,
-# its traffic grew linearly in V (146,188 bytes per vocabulary row, plus
-# 0.150 GB: the chunk's X), and the line gives 22.36 GB at V = 151936.  The
-# other roles' traffic does not grow in proportion at those sizes (W16 leaves
-# L2), so none is reported for them.  The figure holds only for the sources
-# it was captured with: DRAM_BYTES_SOURCES lists the files that decide a GEMM
-# launch's traffic and DRAM_BYTES_DIGEST their SHA-256 at capture time.  When
-# the digest no longer matches, roofline.traffic is reported as null.
-DRAM_BYTES_PER_LAUNCH = {"logits_lse": 22.36e9, "grad_w": None, "grad_x": None, "recomputed_logits_softmax": None}
-DRAM_BYTES_CHUNK_ROWS = 16384  # the chunk size those launches ran with
+# its traffic grew linearly in V (75,716 bytes per vocabulary row, plus
+# 0.047 GB: about the chunk's X), and the line gives 11.55 GB at V = 151936.
+# The figure holds only for the sources it was captured with:
+# DRAM_BYTES_SOURCES lists the files that decide a GEMM launch's traffic and
+# DRAM_BYTES_DIGEST their SHA-256 at capture time.  When the digest no longer
+# matches, roofline.traffic is reported as null.
+DRAM_BYTES_PER_LAUNCH = {"logits_lse": 11.55e9, "grad_w": None, "grad_x": None, "recomputed_logits_softmax": None}
+DRAM_BYTES_CHUNK_ROWS = 8192  # the chunk size those launches ran with
 DRAM_BYTES_FORM = "pair"  # and their GEMM form
 DRAM_BYTES_SOURCES = ["csrc/lce_gemm.cuh", "csrc/lce_gemm_pair.cuh", "csrc/lce_internal.cuh", "csrc/lce_ptx.cuh",
                       "csrc/lce_api.cu", "csrc/lce_gemm_logits.cu", "csrc/lce_gemm_grads.cu"]
-DRAM_BYTES_DIGEST = "297eff2f7ed0a196"
+DRAM_BYTES_DIGEST = "edf7618f947b878b"
 
 
 def gemm_source_digest() -> str:
@@ -549,7 +548,7 @@ def run_ours(args, w):
                      and C == DRAM_BYTES_CHUNK_ROWS and gemm_form == DRAM_BYTES_FORM
                      and gemm_source_digest() == DRAM_BYTES_DIGEST else None,
                      "traffic_source": f"ncu dram__bytes_read.sum + dram__bytes_write.sum of this launch at V = 16384 "
-                                       f"and 32768 (16384-row chunks, H = 4096), scaled linearly in V to the full "
+                                       f"and 32768 (8192-row chunks, H = 4096), scaled linearly in V to the full "
                                        f"vocabulary; sources {DRAM_BYTES_DIGEST} at capture, these sources "
                                        f"{gemm_source_digest()}",
                      "algorithmic_bytes": (2.0 * C * H + 2.0 * V * H + 2.0 * C * V + 4.0 * C * V

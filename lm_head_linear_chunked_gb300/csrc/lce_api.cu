@@ -16,12 +16,16 @@ namespace {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-constexpr int64_t AUTO_CHUNK_ROWS = 16384;
+// Rows per chunk when the caller lets the library choose.  Measured on the
+// Qwen3-8B and Qwen3-4B head shapes against 4096-32768: 8192 rows ran 1.5-2.5%
+// faster than 16384 (and used less energy per step under the power cap)
+// with half the kept-exponential workspace.
+constexpr int64_t AUTO_CHUNK_ROWS = 8192;
 // Smallest chunk whose forward hides the previous chunk's softmax rescale.
 constexpr int64_t OVERLAP_MIN_ROWS = 4096;
 // Tile-order groups: 4096 rows of X (32 MB at H = 4096) for the logits
 // passes, 2048 rows of P for grad_X (single form); for the grad_W pass, as
-// many 256-column tiles of the fp16 X chunk as make about 32 MB (4 at 16384
+// many 256-column tiles of the fp16 X chunk as make about 32 MB (8 at 8192
 // rows), or 64 MB in the pair form.
 constexpr int64_t LOGITS_GROUP_ROWS = 4096;
 constexpr int64_t GRADX_GROUP_ROWS = 2048;

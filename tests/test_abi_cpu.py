@@ -67,8 +67,8 @@ def test_status_strings():
     assert lce.lce_status_string(99) == "unknown status"
 
 
-@pytest.mark.parametrize("N,chunk,expect", [(512, 256, 256), (512, 0, 512), (100000, 0, 16384), (7, 1000, 7),
-                                            (131072, 0, 16384), (4096, 1, 1)])
+@pytest.mark.parametrize("N,chunk,expect", [(512, 256, 256), (512, 0, 512), (100000, 0, 8192), (7, 1000, 7),
+                                            (131072, 0, 8192), (4096, 1, 1)])
 def test_chunk_rows(N, chunk, expect):
     assert lce.lce_chunk_rows(N, 1024, 32768, chunk) == expect
 
@@ -78,7 +78,7 @@ def test_workspace_sizes():
     f = lce.lce_workspace_size(N, H, V, 0, False, lce.WS_FORWARD)
     b = lce.lce_workspace_size(N, H, V, 0, False, lce.WS_BACKWARD)
     fb = lce.lce_workspace_size(N, H, V, 0, False, lce.WS_FUSED)
-    C, ldg, n_vt = 16384, V, -(-V // 256)
+    C, ldg, n_vt = 8192, V, -(-V // 256)
     second = C * ldg * 2 + 2 * n_vt * C * 4        # the overlapped chunk's E and half-tile maxes
     assert fb >= max(f, b) and fb <= f + b + second
     assert b >= C * V * 2                          # one chunk of fp16 P
