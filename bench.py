@@ -512,8 +512,11 @@ def run_ours(args, w):
     # tensor-core FLOPs the step executes: 2NHV per GEMM role that ran
     executed = sum(2.0 * N * H * V for k in gemm_kinds if prof[k][1] > 0)
     dom_ms, dom_n = prof[dom]
+    # each GEMM role runs once per chunk; a split grad_X product adds its
+    # reduction kernel to the role, so time is counted per chunk, not per launch
+    role_chunks = args.steps * n_chunks
     dom_flops_per_launch = 2.0 * N * H * V / n_chunks
-    dom_tflops = dom_flops_per_launch / (dom_ms / dom_n / 1e3) / 1e12
+    dom_tflops = dom_flops_per_launch / (dom_ms / role_chunks / 1e3) / 1e12
     sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     total_launches = sum(v[1] for v in prof.values())
@@ -556,12 +559,15 @@ def run_ours(args, w):
                      "kernel": f"{'gemm_pair_kernel' if gemm_form == 'pair' else 'gemm_kernel'} ({dom})" + (
                          ", which also turns the previous chunk's kept exponentials into the softmax (4*C*V bytes) "
                          "with its epilogue warps" if dom == "logits_lse" and overlapped else ""),
-                     "roles": {k: {"tflops": 2.0 * N * H * V / n_chunks / (prof[k][0] / prof[k][1] / 1e3) / 1e12,
-                                   "frac": 2.0 * N * H * V / n_chunks / (prof[k][0] / prof[k][1] / 1e3) / 1e12 /
-                                   sustained, "mean_launch_ms": prof[k][0] / prof[k][1]}
+                     "roles": {k: {"tflops": 2.0 * N * H * V / n_chunks / (prof[k][0] / role_chunks / 1e3) / 1e12,
+                                   "frac": 2.0 * N * H * V / n_chunks / (prof[k][0] / role_chunks / 1e3) / 1e12 /
+                                   sustained, "ms_per_chunk": prof[k][0] / role_chunks,
+                                   "launches_per_chunk": prof[k][1] / role_chunks}
                                for k in gemm_kinds if prof[k][1] > 0},
+                     "roles_note": "per chunk: the role's GEMM launch and, for grad_x, the kernel that adds the "
+                                   "partial sums of a product split over the vocabulary",
                      "flops_per_launch": dom_flops_per_launch, "launches": dom_n,
-                     "mean_launch_ms": dom_ms / dom_n,
+                     "mean_launch_ms": dom_ms / role_chunks,
                      "peak_source": f"{peak_src} sustained bf16 (fp16 operands run at the bf16 rate)"},
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
         "profiled_pass": {"value": replica_rate(N, ws_n, t_prof), "ms_per_step": 1e3 * t_prof,

@@ -23,6 +23,7 @@ __all__ = [
     "LCEError", "IGNORE_INDEX", "WS_FORWARD", "WS_BACKWARD", "WS_FUSED", "WS_FUSED_MIN", "STATUS", "library_path", "lib",
     "lce_workspace_size", "lce_chunk_rows", "lce_forward", "lce_backward", "lce_fused_fwd_bwd",
     "lce_check_status", "lce_status_string", "lce_debug_gemm", "lce_debug_wait_timeout",
+    "lce_debug_gradx_tail_plan",
     "lce_profile_begin", "lce_profile_end", "PROFILE_KINDS", "lce_forward_static_ws", "STATIC_SCRATCH_BYTES",
     "lce_static_ws_check_status",
     "lce_scale_grads",
@@ -66,6 +67,7 @@ _SIGS = {
     "lce_status_string": [_STATUS],
     "lce_debug_gemm": [ctypes.c_int, _I64, _I64, _I64, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "lce_debug_wait_timeout": [ctypes.c_uint32, _P, ctypes.c_size_t, _P],
+    "lce_debug_gradx_tail_plan": [_I64, _I64, _I64, ctypes.POINTER(_I64)],
     "lce_forward_static_ws": [_I64, _I64, _I64, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _P],
     "lce_static_ws_check_status": [_P],
     "lce_scale_grads": [_I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P],
@@ -238,6 +240,14 @@ def lce_debug_gemm(layout, M, N, K, A, B, D, ws, ws_bytes, stream) -> None:
 
 def lce_debug_wait_timeout(limit_us, ws, ws_bytes, stream) -> None:
     _check(lib().lce_debug_wait_timeout(limit_us, _ptr(ws), ws_bytes, _stream(stream)), "lce_debug_wait_timeout")
+
+
+def lce_debug_gradx_tail_plan(tiles, slots, k_blocks) -> tuple:
+    """(tiles computed whole, tiles split over K after them, slices per split
+    tile, k-blocks per slice) of a pair-form grad_X launch."""
+    out = (_I64 * 4)()
+    _check(lib().lce_debug_gradx_tail_plan(tiles, slots, k_blocks, out), "lce_debug_gradx_tail_plan")
+    return tuple(int(v) for v in out)
 
 
 GEMM_SINGLE, GEMM_PAIR = 0, 1

@@ -63,7 +63,7 @@ struct Plan {
     // half-tile-max buffers)
     bool overlap;
     size_t off_row_loss, off_zt, off_pm, off_ps, off_g, off_gb, off_keys, off_runs, off_nrun, off_lcsum, off_w16,
-        off_x16, off_dmap, off_crow, off_nvc, off_split, off_g2, off_pm2, off_tcoef, total;
+        off_x16, off_dmap, off_crow, off_nvc, off_split, off_g2, off_pm2, off_tcoef, off_tail, total;
 };
 
 lce_status_t check_sizes(int64_t N, int64_t H, int64_t V, int64_t chunk_rows) {
@@ -125,6 +125,8 @@ lce_status_t make_plan(int64_t N, int64_t H, int64_t V, int64_t chunk_rows, bool
     p->off_g2 = take(p->overlap, static_cast<size_t>(p->C) * p->ldg * 2);
     p->off_pm2 = take(p->overlap, static_cast<size_t>(2 * p->n_vt) * p->C * 4);
     p->off_tcoef = take(bwd, static_cast<size_t>(N) * 4);  // c_i = p_{i,y_i} - 1 of every row
+    // grad_X's split tail tiles (pair form, chunks not split over K as a whole)
+    p->off_tail = take(bwd && p->gradx_splits <= 1, static_cast<size_t>(TAIL_UNITS_MAX) * TAIL_TILE_FLOATS * 4);
     p->total = off;
     return LCE_OK;
 }
@@ -358,6 +360,7 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
     float* tcoef = do_bwd ? reinterpret_cast<float*>(wsb + p.off_tcoef) : nullptr;
     uint16_t* G2 = p.overlap ? reinterpret_cast<uint16_t*>(wsb + p.off_g2) : nullptr;
     float* pm2 = p.overlap ? reinterpret_cast<float*>(wsb + p.off_pm2) : nullptr;
+    float* tail = (do_bwd && p.gradx_splits <= 1 && form.pair) ? reinterpret_cast<float*>(wsb + p.off_tail) : nullptr;
 
     // every GEMM launch of the call: the extents the bounds-checking build checks against
     auto call_args = [&]() {
@@ -509,10 +512,17 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             a.k_per_split = static_cast<int32_t>(cdiv(a.k_blocks, p.gradx_splits));
             a.split_out = split_out;
             a.split_stride = p.C * pb.H;
-            LCE_LAUNCH(PK_GRADX, launch_gemm(MODE_GRADX, mG_k, mW16_mn, mW16_mn, a,
-                                             grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles *
-                                                               p.gradx_splits),
-                                             s, form.pair));
+            a.tail_out = tail;
+            a.tail_units_max = TAIL_UNITS_MAX;
+            // with the tail split, a chunk of fewer tiles than pairs still gets every
+            // pair: its slices spread over them
+            const int grid = grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles *
+                                               (tail ? TAIL_SPLIT_MAX : p.gradx_splits));
+            LCE_LAUNCH(PK_GRADX, launch_gemm(MODE_GRADX, mG_k, mW16_mn, mW16_mn, a, grid, s, form.pair));
+            if (tail)  // the same plan as the GEMM's: its pairs, tile columns and K extent
+                LCE_LAUNCH(PK_GRADX, launch_gradx_tail_reduce(tail, grid / 2, a.n_tiles, a.k_blocks, pb.H, crow + r0,
+                                                              nvc + c, rows, pb.y + r0, pb.ignore_index, pb.V, pb.W,
+                                                              tcoef + r0, hdr, o.grad_X + r0 * pb.H, s));
             if (split_out)
                 LCE_LAUNCH(PK_GRADX, launch_gradx_split_reduce(split_out, p.gradx_splits, p.C * pb.H, pb.H, crow + r0,
                                                                nvc + c, rows, pb.y + r0, pb.ignore_index, pb.V,
@@ -808,6 +818,19 @@ int lce_gemm_pair_slots(void) { return gemm_pair_slots(); }
 int lce_set_gemm_form(int form) {
     if (form != LCE_GEMM_SINGLE && form != LCE_GEMM_PAIR) return -1;
     return g_gemm_form.exchange(form);
+}
+
+lce_status_t lce_debug_gradx_tail_plan(int64_t tiles, int64_t slots, int64_t k_blocks, int64_t out[4]) {
+    if (!out || tiles < 0 || slots < 0 || k_blocks < 0 || tiles > INT32_MAX || slots > INT32_MAX ||
+        k_blocks > INT32_MAX)
+        return LCE_ERR_INVALID_ARG;
+    const TailPlan tp =
+        gradx_tail_plan(static_cast<int>(tiles), static_cast<int>(slots), static_cast<int>(k_blocks));
+    out[0] = tp.full;
+    out[1] = tp.tail;
+    out[2] = tp.s;
+    out[3] = tp.kps;
+    return LCE_OK;
 }
 
 lce_status_t lce_debug_wait_timeout(uint32_t limit_us, void* ws, size_t ws_bytes, lce_stream_t stream) {

@@ -576,10 +576,52 @@ __global__ void scale_grads_kernel(int64_t nx8, int64_t nw8, int64_t V, const fl
         }
 }
 
+// grad_X[crow[j], h .. h+8] = s (f' sum + c W[y, h]) as bf16 from a compacted
+// row's summed K slices (f = s 2^-(15+k_W)): the arithmetic of the unsplit
+// epilogue.
+__device__ __forceinline__ void gradx_finish8(const float (&sum)[8], int64_t j, int64_t h, int64_t H, float s,
+                                              float f, const int* __restrict__ crow, const int64_t* __restrict__ y,
+                                              int64_t ignore_index, int64_t V, const uint16_t* __restrict__ W,
+                                              const float* __restrict__ tcoef, const WsHeader* hdr,
+                                              uint16_t* __restrict__ grad_X_chunk, int64_t max_rows) {
+    const int64_t r = crow[j];
+    if (!LCE_IN(r >= 0 && r < max_rows, const_cast<unsigned*>(&hdr->status))) return;
+    const int64_t yr = y[r];
+    float w[8];
+    const bool valid = yr != ignore_index && yr >= 0 && yr < V;
+    const float sc = valid ? s * tcoef[r] : 0.f;
+    if (valid) {
+        const uint4 q = *reinterpret_cast<const uint4*>(W + yr * H + h);
+        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            w[2 * k] = __uint_as_float(u[k] << 16);
+            w[2 * k + 1] = __uint_as_float(u[k] & 0xFFFF0000u);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = 0.f;
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(fmaf(f, sum[2 * k], sc * w[2 * k]),
+                                                  fmaf(f, sum[2 * k + 1], sc * w[2 * k + 1]));
+        o[k] = *reinterpret_cast<uint32_t*>(&b2);
+    }
+    *reinterpret_cast<uint4*>(grad_X_chunk + r * H + h) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ void add8(float (&sum)[8], const float* src) {
+    const float4 a = *reinterpret_cast<const float4*>(src);
+    const float4 b = *reinterpret_cast<const float4*>(src + 4);
+    sum[0] += a.x; sum[1] += a.y; sum[2] += a.z; sum[3] += a.w;
+    sum[4] += b.x; sum[5] += b.y; sum[6] += b.z; sum[7] += b.w;
+}
+
 // Finishes a split grad_X product: for each compacted row j < n_valid and
-// column h, sum the K slices' partial sums in slice order, then
-// grad_X[crow[j], h] = s (2^-(15+k_W) sum + c W[y, h]) as bf16 (the same
-// arithmetic as the unsplit epilogue).
+// column h, sum the K slices' partial sums in slice order, then finish as
+// the unsplit epilogue does.
 __global__ void gradx_split_reduce_kernel(const float* __restrict__ split_out, int64_t splits, int64_t split_stride,
                                           int64_t H, const int* __restrict__ crow, const int* __restrict__ n_valid,
                                           const int64_t* __restrict__ y, int64_t ignore_index, int64_t V,
@@ -595,39 +637,47 @@ __global__ void gradx_split_reduce_kernel(const float* __restrict__ split_out, i
         float sum[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) sum[k] = 0.f;
-        for (int64_t ks = 0; ks < splits; ++ks) {
-            const float* src = split_out + ks * split_stride + j * H + h;
-            const float4 a = *reinterpret_cast<const float4*>(src);
-            const float4 b = *reinterpret_cast<const float4*>(src + 4);
-            sum[0] += a.x; sum[1] += a.y; sum[2] += a.z; sum[3] += a.w;
-            sum[4] += b.x; sum[5] += b.y; sum[6] += b.z; sum[7] += b.w;
-        }
-        const int64_t r = crow[j];
-        if (!LCE_IN(r >= 0 && r < max_rows, const_cast<unsigned*>(&hdr->status))) continue;
-        const int64_t yr = y[r];
-        float w[8];
-        const bool valid = yr != ignore_index && yr >= 0 && yr < V;
-        const float sc = valid ? s * tcoef[r] : 0.f;
-        if (valid) {
-            const uint4 q = *reinterpret_cast<const uint4*>(W + yr * H + h);
-            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+        for (int64_t ks = 0; ks < splits; ++ks) add8(sum, split_out + ks * split_stride + j * H + h);
+        gradx_finish8(sum, j, h, H, s, f, crow, y, ignore_index, V, W, tcoef, hdr, grad_X_chunk, max_rows);
+    }
+}
+
+// Finishes the split tail tiles of a grad_X launch of the pair form: the
+// plan is recomputed from the chunk's valid rows as the GEMM computed it;
+// for each tail tile's valid row and column, the slices' partial tiles are
+// summed in slice order, then finished as the unsplit epilogue does.  One
+// thread per 8 columns of a row, consecutive threads along the row.
+__global__ void gradx_tail_reduce_kernel(const float* __restrict__ tail_out, int slots, int n_tiles, int k_blocks,
+                                         int64_t H, const int* __restrict__ crow, const int* __restrict__ n_valid,
+                                         const int64_t* __restrict__ y, int64_t ignore_index, int64_t V,
+                                         const uint16_t* __restrict__ W, const float* __restrict__ tcoef,
+                                         const WsHeader* hdr, uint16_t* __restrict__ grad_X_chunk,
+                                         int64_t max_rows) {
+    const int64_t nv = *n_valid;
+    const TailPlan tp =
+        gradx_tail_plan(static_cast<int>((nv + 2 * BM - 1) / (2 * BM)) * n_tiles, slots, k_blocks);
+    if (tp.tail == 0) return;
+    if (!LCE_IN(static_cast<int64_t>(tp.tail) * tp.s <= TAIL_UNITS_MAX, const_cast<unsigned*>(&hdr->status)))
+        return;
+    const float s = hdr->scale;
+    const float f = ldexpf(s, -(P_SCALE_EXP + operand_scale_exp(hdr->amax_w_bits)));
+    constexpr int G = BN / 8;  // 8-column groups per tile row
+    const int64_t total = static_cast<int64_t>(tp.tail) * (2 * BM) * G;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total; e += stride) {
+        const int i = static_cast<int>(e / ((2 * BM) * G));
+        const int rem = static_cast<int>(e - static_cast<int64_t>(i) * (2 * BM) * G);
+        const int tr = rem / G, g = rem - tr * G;
+        const int t = tp.full + i;  // tile order n fastest: tile t is (t / n_tiles, t % n_tiles)
+        const int64_t j = static_cast<int64_t>(t / n_tiles) * (2 * BM) + tr;
+        const int64_t h = static_cast<int64_t>(t % n_tiles) * BN + 8 * g;
+        if (j >= nv || h >= H) continue;
+        float sum[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                w[2 * k] = __uint_as_float(u[k] << 16);
-                w[2 * k + 1] = __uint_as_float(u[k] & 0xFFFF0000u);
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) w[k] = 0.f;
-        }
-        uint32_t o[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(fmaf(f, sum[2 * k], sc * w[2 * k]),
-                                                      fmaf(f, sum[2 * k + 1], sc * w[2 * k + 1]));
-            o[k] = *reinterpret_cast<uint32_t*>(&b2);
-        }
-        *reinterpret_cast<uint4*>(grad_X_chunk + r * H + h) = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int k = 0; k < 8; ++k) sum[k] = 0.f;
+        for (int ks = 0; ks < tp.s; ++ks)
+            add8(sum, tail_out + (static_cast<int64_t>(ks) * tp.tail + i) * TAIL_TILE_FLOATS + tr * BN + 8 * g);
+        gradx_finish8(sum, j, h, H, s, f, crow, y, ignore_index, V, W, tcoef, hdr, grad_X_chunk, max_rows);
     }
 }
 
@@ -835,6 +885,18 @@ cudaError_t launch_scale_grads(int64_t N, int64_t H, int64_t V, const float* d_g
                                               reinterpret_cast<uint4*>(grad_X),
                                               reinterpret_cast<const float4*>(grad_W_acc),
                                               reinterpret_cast<uint4*>(grad_W), grad_b_acc, grad_b);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gradx_tail_reduce(const float* tail_out, int slots, int n_tiles, int k_blocks, int64_t H,
+                                     const int* crow, const int* n_valid, int64_t max_rows, const int64_t* y,
+                                     int64_t ignore_index, int64_t V, const uint16_t* W, const float* tcoef,
+                                     const WsHeader* hdr, uint16_t* grad_X_chunk, cudaStream_t s) {
+    // at most slots - 1 tail tiles of 256 rows x 32 groups of 8 columns
+    const int64_t want = (static_cast<int64_t>(slots) * 2 * BM * (BN / 8) + 255) / 256;
+    const int blocks = static_cast<int>(want < 1 ? 1 : (want < 1216 ? want : 1216));
+    gradx_tail_reduce_kernel<<<blocks, 256, 0, s>>>(tail_out, slots, n_tiles, k_blocks, H, crow, n_valid, y,
+                                                    ignore_index, V, W, tcoef, hdr, grad_X_chunk, max_rows);
     return cudaGetLastError();
 }
 

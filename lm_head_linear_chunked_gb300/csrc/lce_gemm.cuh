@@ -103,6 +103,29 @@ __device__ __forceinline__ void tile_and_slice(int t, const GemmArgs& a, int& m,
     tile_coords(t - ks * per, a, m, n);
 }
 
+// Work unit u of a launch: output tile (m, n), K slice ks and its k-block
+// range [kb0, kb1), and tj = the partial-tile index of a split tail unit
+// (-1 otherwise).  With a tail plan (tp.tail > 0) the first tp.full units
+// are whole tiles and unit tp.full + j is slice j / tp.tail of tile
+// tp.full + j % tp.tail, so one round of units takes every tail tile's
+// slice before the next slice of any.
+__device__ __forceinline__ void unit_coords(int u, const GemmArgs& a, const TailPlan& tp, int k_blocks, int& m,
+                                            int& n, int& ks, int& kb0, int& kb1, int& tj) {
+    tj = -1;
+    if (tp.tail > 0 && u >= tp.full) {
+        const int j = u - tp.full;
+        ks = j / tp.tail;
+        tile_coords(tp.full + (j - ks * tp.tail), a, m, n);
+        kb0 = ks * tp.kps;
+        kb1 = min(k_blocks, kb0 + tp.kps);
+        tj = j;
+        return;
+    }
+    tile_and_slice(u, a, m, n, ks);
+    kb0 = a.k_splits > 1 ? ks * a.k_per_split : 0;
+    kb1 = a.k_splits > 1 ? min(k_blocks, kb0 + a.k_per_split) : k_blocks;
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -306,7 +329,7 @@ template <int MODE, bool PAIR = false>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, int q, int half, int lane,
                                               uint32_t taddr, uint32_t empty_bar, int64_t m_rows,
                                               bool zero_acc, int ks, const float4 (&pre)[8], float* stage,
-                                              const CUtensorMap* map_c) {
+                                              const CUtensorMap* map_c, int tj = -1) {
     const int64_t row = static_cast<int64_t>(m) * BM + q * 32 + lane;
     const int64_t col0 = static_cast<int64_t>(n) * BN;
     const int j0 = half * (BN / 64);  // this warp's four 32-column chunks: half of the tile's columns
@@ -431,10 +454,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         if (row_ok && a.part_s && LCE_IN(2 * n + half < a.cap_pt && row < a.ldp, a.status))
             a.part_s[(2 * static_cast<int64_t>(n) + half) * a.ldp + row] = se;
     } else if constexpr (MODE == MODE_GRADX) {
-      if (a.k_splits > 1) {
+      if (a.k_splits > 1 || tj >= 0) {
         // one K slice of a split product: the raw fp32 partial sums, finished
-        // by the reduction kernel (fixed slice order)
-        float* dst = a.split_out + static_cast<int64_t>(ks) * a.split_stride;
+        // by a reduction kernel (fixed slice order).  A split tail unit's
+        // slice goes to its own 256 x 256 partial tile (the pair tile's row,
+        // this column), the k_splits form's to the slice's rows of the chunk.
+        const bool tail = tj >= 0;
+        const int64_t trow = row - static_cast<int64_t>(m >> 1) * (2 * BM);  // row within the pair tile
+        float* dst = tail ? a.tail_out + static_cast<int64_t>(tj) * TAIL_TILE_FLOATS + trow * BN
+                          : a.split_out + static_cast<int64_t>(ks) * a.split_stride + row * a.N;
+        const int64_t cbase = tail ? col0 : 0;  // dst's first column
+        // rows past the valid ones are not stored (and not checked)
+        const bool store = row_ok && (tail ? LCE_IN(PAIR && tj < a.tail_units_max && trow >= 0 && trow < 2 * BM,
+                                                    a.status)
+                                           : LCE_IN(ks < a.k_splits && row < a.cap_rows, a.status));
 #pragma unroll 1
         for (int j = j0; j < j0 + BN / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
@@ -445,8 +478,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = 0.f;
             }
-            if (row_ok && LCE_IN(ks < a.k_splits && row < a.cap_rows, a.status))
-                store_f32_32(dst + row * a.N + c0, v, static_cast<int>(min64(32, a.N - c0)));
+            if (store) store_f32_32(dst + (c0 - cbase), v, static_cast<int>(min64(32, a.N - c0)));
         }
         tc_fence_before_sync();
         __syncwarp();

@@ -118,6 +118,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const int dyn = args.dyn_rows ? *args.dyn_rows : -1;
     const int64_t m_rows = (MODE == MODE_GRADX && dyn >= 0) ? static_cast<int64_t>(dyn) : args.M;
     const int k_blocks = (MODE == MODE_GRADW && dyn >= 0) ? (dyn + BK - 1) / BK : args.k_blocks;
+    // grad_X: the last partial round of tiles split over K.  With n fastest in
+    // the tile order, the tiles that hold valid rows are the first ones.
+    TailPlan tp{num_tiles, 0, 1, k_blocks};
+    int num_units = num_tiles;
+    if (MODE == MODE_GRADX && args.tail_out && args.k_splits <= 1 && args.raster == 1) {
+        tp = gradx_tail_plan(static_cast<int>((m_rows + PAIR_BM - 1) / PAIR_BM) * args.n_tiles, ncl, k_blocks);
+        num_units = tp.full + tp.tail * tp.s;
+    }
 
     if (warp == 0) {
         if (lane == 0) {
@@ -125,12 +133,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             uint32_t stage = 0, phase = 0;
             uint64_t issued = 0;
             bool ok = true;
-            for (int t = cid; t < num_tiles && ok; t += ncl) {
-                int m, n, ks;
-                tile_and_slice(t, args, m, n, ks);
+            for (int t = cid; t < num_units && ok; t += ncl) {
+                int m, n, ks, kb0, kb1, tj;
+                unit_coords(t, args, tp, k_blocks, m, n, ks, kb0, kb1, tj);
                 if (static_cast<int64_t>(m) * PAIR_BM >= m_rows) continue;
-                const int kb0 = args.k_splits > 1 ? ks * args.k_per_split : 0;
-                const int kb1 = args.k_splits > 1 ? min(k_blocks, kb0 + args.k_per_split) : k_blocks;
                 const int32_t arow = m * PAIR_BM + static_cast<int32_t>(rank) * BM;
                 const int32_t bcol = n * BN + static_cast<int32_t>(rank) * (BN / 2);
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -206,12 +212,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             constexpr uint32_t B_STEP = T::B_MN ? (2048u >> 4) : (32u >> 4);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = cid; t < num_tiles && ok; t += ncl) {
-                int m, n, ks;
-                tile_and_slice(t, args, m, n, ks);
+            for (int t = cid; t < num_units && ok; t += ncl) {
+                int m, n, ks, kb0, kb1, tj;
+                unit_coords(t, args, tp, k_blocks, m, n, ks, kb0, kb1, tj);
                 if (static_cast<int64_t>(m) * PAIR_BM >= m_rows) continue;
-                const int kb0 = args.k_splits > 1 ? ks * args.k_per_split : 0;
-                const int kb1 = args.k_splits > 1 ? min(k_blocks, kb0 + args.k_per_split) : k_blocks;
                 if (!wait_phase_pair(smem_u32(&ctl->tmem_empty[acc]), acc_phase ^ 1u, ctl, peer_abort, args.status,
                                      limit)) {
                     ok = false;
@@ -259,12 +263,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         if constexpr (MODE == MODE_LSE)
             side_init(args, side, static_cast<int64_t>(blockIdx.x) * EPI_WARPS + (warp - 2),
                       static_cast<int64_t>(gridDim.x) * EPI_WARPS, (num_tiles - cid + ncl - 1) / ncl);
-        for (int t = cid; t < num_tiles; t += ncl) {
-            int m, n, ks;
-            tile_and_slice(t, args, m, n, ks);
+        for (int t = cid; t < num_units; t += ncl) {
+            int m, n, ks, kb0, kb1, tj;
+            unit_coords(t, args, tp, k_blocks, m, n, ks, kb0, kb1, tj);
             if (static_cast<int64_t>(m) * PAIR_BM >= m_rows) continue;
-            const int kb0 = args.k_splits > 1 ? ks * args.k_per_split : 0;
-            const int kb1 = args.k_splits > 1 ? min(k_blocks, kb0 + args.k_per_split) : k_blocks;
             const int mc = 2 * m + static_cast<int>(rank);  // this CTA's 128-row tile
             float4 pre[8];
             if constexpr (MODE == MODE_GRADW) {
@@ -278,7 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             epilogue_tile<MODE, true>(args, mc, n, q, half, lane, taddr,
                                       map_shared_rank(smem_u32(&ctl->tmem_empty[acc]), 0), m_rows, kb1 <= kb0, ks,
-                                      pre, epi_stage, &map_c);
+                                      pre, epi_stage, &map_c, tj);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
             if constexpr (MODE == MODE_LSE) side_work(args, side, lane, side.budget);

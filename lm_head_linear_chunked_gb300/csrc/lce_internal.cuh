@@ -75,6 +75,50 @@ constexpr int gemm_smem_bytes(int mode, bool pair) {
 static_assert(GEMM_SMEM_BYTES + EPI_STAGE_BYTES <= 232448 && GEMM_PAIR_SMEM_BYTES + EPI_STAGE_BYTES <= 232448,
               "shared memory of one CTA");
 
+// grad_X's last partial wave (pair form).  Each grad_X tile runs the whole
+// vocabulary as its K loop (about a millisecond at V = 151936), so when a
+// launch's tiles leave the last round of pairs partly filled, the idle pairs
+// wait a whole tile.  The plan keeps the whole rounds of tiles as they are
+// and splits each of the r tiles after them into s K slices, dealt out to
+// the pairs like tiles; each slice's raw FP32 sum goes to a partial tile of
+// the workspace, and a reduction kernel finishes those tiles, adding the
+// slices in slice order.  s is the one of 2..TAIL_SPLIT_MAX that makes the
+// tail's rounds of slices, ceil(r s / slots) / s of a tile, shortest; no split
+// unless that saves at least an eighth of a tile.
+struct TailPlan {
+    int32_t full;   // tiles computed whole: the first `full` tiles of the launch's tile order
+    int32_t tail;   // tiles split over K after them (0: no split)
+    int32_t s;      // K slices per split tile
+    int32_t kps;    // k-blocks per slice (the last slice may be shorter; none is empty)
+};
+constexpr int TAIL_SPLIT_MAX = 8;
+constexpr int TAIL_UNITS_MAX = 320;     // tail x s partial tiles of 256 x 256 FP32 (80 MB of workspace)
+constexpr int TAIL_MIN_KBLOCKS = 16;    // shortest slice, in 64-wide k-blocks
+constexpr int64_t TAIL_TILE_FLOATS = static_cast<int64_t>(2 * BM) * BN;
+
+// n_act: output tiles with valid rows; slots: pairs of the launch.
+__host__ __device__ inline TailPlan gradx_tail_plan(int n_act, int slots, int k_blocks) {
+    TailPlan p{n_act > 0 ? n_act : 0, 0, 1, k_blocks};
+    if (n_act <= 0 || slots <= 0) return p;
+    const int r = n_act % slots;
+    if (r == 0) return p;
+    int best = 1, best_rounds = 1;  // tail time = best_rounds / best tiles
+    for (int s = 2; s <= TAIL_SPLIT_MAX; ++s) {
+        if (r * s > TAIL_UNITS_MAX || k_blocks < s * TAIL_MIN_KBLOCKS) break;
+        const int rounds = (r * s + slots - 1) / slots;
+        if (rounds * best < best_rounds * s) {
+            best = s;
+            best_rounds = rounds;
+        }
+    }
+    if (best == 1 || 8 * best_rounds > 7 * best) return p;
+    p.kps = (k_blocks + best - 1) / best;
+    p.s = (k_blocks + p.kps - 1) / p.kps;
+    p.full = n_act - r;
+    p.tail = r;
+    return p;
+}
+
 // Device status word bits (bit k set = lce_status_t k was raised).
 constexpr unsigned STATUS_LABEL = 1u << LCE_ERR_LABEL_RANGE;
 constexpr unsigned STATUS_TIMEOUT = 1u << LCE_ERR_TIMEOUT;
@@ -189,6 +233,13 @@ struct GemmArgs {
     int32_t k_per_split;
     float* split_out;
     int64_t split_stride;
+    // MODE_GRADX, pair form, no k_splits: split the last partial round of
+    // tiles over K (gradx_tail_plan of the valid rows' tiles and the
+    // launch's pairs).  Split unit j (< tail_units_max) writes its raw FP32
+    // sum to tail_out[j] (a 256 x 256 tile, row stride 256); unit j is slice
+    // j / tail of tile full + j % tail.  nullptr: no split.
+    float* tail_out;
+    int32_t tail_units_max;
     // MODE_LSE side job (fused call): between tiles, the epilogue warps turn
     // the previous chunk's kept exponentials E into P in place, the work of
     // p_rescale_kernel, in units of 8 compact rows x one 256-column vocab
@@ -274,6 +325,12 @@ cudaError_t launch_gradx_split_reduce(const float* split_out, int64_t splits, in
                                       const int* crow, const int* n_valid, int64_t max_rows, const int64_t* y,
                                       int64_t ignore_index, int64_t V, const uint16_t* W, const float* tcoef,
                                       const WsHeader* hdr, uint16_t* grad_X_chunk, cudaStream_t s);
+// Finishes the split tail tiles of one grad_X launch of the pair form (slots:
+// its pairs; n_tiles, k_blocks: its tile columns and K extent).
+cudaError_t launch_gradx_tail_reduce(const float* tail_out, int slots, int n_tiles, int k_blocks, int64_t H,
+                                     const int* crow, const int* n_valid, int64_t max_rows, const int64_t* y,
+                                     int64_t ignore_index, int64_t V, const uint16_t* W, const float* tcoef,
+                                     const WsHeader* hdr, uint16_t* grad_X_chunk, cudaStream_t s);
 cudaError_t launch_amax(const uint16_t* x, int64_t n, unsigned* amax_bits, cudaStream_t s);
 cudaError_t launch_to_f16_scaled(const uint16_t* x, int64_t n, const unsigned* amax_bits, uint16_t* out,
                                  cudaStream_t s);

@@ -216,3 +216,50 @@ def test_reduction_names_are_checked():
     assert lce._flags("mean", False) == 0
     with pytest.raises(ValueError):
         lce._flags("none", False)
+
+
+@pytest.mark.parametrize("tiles,slots,kb,want", [
+    (496, 76, 2374, (456, 40, 7, 340)),   # 8192-row chunk, 7782 valid rows, H = 4096, V = 151936
+    (456, 76, 2374, (456, 0, 1, 2374)),   # whole rounds: nothing to split
+    (151, 76, 2374, (151, 0, 1, 2374)),   # 75 tiles in the last round: no split saves an eighth of a tile
+    (40, 76, 20, (40, 0, 1, 20)),         # K too short to split
+    (0, 76, 100, (0, 0, 1, 100)),         # no valid rows
+    (32, 76, 64, (0, 32, 2, 32)),         # fewer tiles than pairs: all of them split
+    (5, 0, 64, (5, 0, 1, 64)),
+])
+def test_gradx_tail_plan(tiles, slots, kb, want):
+    assert lce.lce_debug_gradx_tail_plan(tiles, slots, kb) == want
+
+
+def test_gradx_tail_plan_properties():
+    """On random launches: the slices cover K without an empty one, the
+    partial tiles fit the workspace's 320, and the split taken is the
+    shortest tail among the allowed ones (none when none saves an eighth)."""
+    rng = __import__("random").Random(5)
+
+    def tail_time(r, s, slots):
+        return -(-r * s // slots) / s
+
+    for _ in range(3000):
+        slots = rng.choice([1, 2, 37, 75, 76, 80, 148])
+        tiles = rng.randrange(0, 6 * slots + 3)
+        kb = rng.choice([1, 15, 32, 64, 127, 128, 2374, rng.randrange(1, 3000)])
+        full, tail, s, kps = lce.lce_debug_gradx_tail_plan(tiles, slots, kb)
+        r = tiles % slots
+        allowed = [t for t in range(2, 9) if r * t <= 320 and kb >= 16 * t]
+        good = [t for t in allowed if 8 * -(-r * t // slots) <= 7 * t]
+        if tail == 0:
+            assert (full, s, kps) == (tiles, 1, kb)
+            assert r == 0 or not good
+            continue
+        assert full + tail == tiles and full % slots == 0 and tail == r
+        assert 2 <= s <= 8 and tail * s <= 320 and (s - 1) * kps < kb <= s * kps and kps >= 16
+        assert 8 * -(-tail * s // slots) <= 7 * s
+        assert all(tail_time(r, s, slots) <= tail_time(r, t, slots) for t in allowed)
+
+
+def test_gradx_tail_plan_rejects():
+    for args in [(-1, 76, 10), (10, -1, 10), (10, 76, -1), (2**31, 76, 10)]:
+        with pytest.raises(lce.LCEError) as e:
+            lce.lce_debug_gradx_tail_plan(*args)
+        assert e.value.status == 1
