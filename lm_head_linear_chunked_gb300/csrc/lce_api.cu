@@ -544,7 +544,9 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             a.ld_out = pb.H;
             a.acc_first = first;
             a.write_bf16 = last && o.grad_W != nullptr;
-            a.acc_tma = 1;
+            // pair form with whole 256-column tiles: later chunks read the old
+            // accumulator blocks by TMA and store them back (plain streams)
+            a.acc_tma = (form.pair && pb.H % BN == 0) ? 2 : 1;
             a.b_amax_bits = &hdr->amax_x_bits;
             a.dyn_rows = nvc + c;
             LCE_LAUNCH(PK_GRADW, launch_gemm(MODE_GRADW, mG_mn, mX16_mn, mAcc, a,

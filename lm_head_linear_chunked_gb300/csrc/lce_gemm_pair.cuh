@@ -32,6 +32,7 @@ struct SharedCtlPair {
     uint64_t tmem_empty[2];
     uint64_t drain;
     uint64_t fin;
+    uint64_t old_full[EPI_WARPS][GRADW_PAIR_BUFS];  // grad_W (acc_tma 2): an old accumulator block has landed
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -57,6 +58,101 @@ __device__ __forceinline__ bool wait_phase_pair(uint32_t bar, uint32_t parity, S
     }
 }
 
+// grad_W's read-modify-write of the FP32 accumulator in the chunks between
+// the first and the last (acc_tma 2).  Each epilogue warp streams its 32x32
+// blocks through its GRADW_PAIR_BUFS 4 KB buffers: the old values arrive by
+// TMA load that many blocks ahead, the lanes add s times the accumulator in
+// place, and a TMA store writes the block back.  Block g of a warp is
+// 32-column slab g & 3 of its half of the tile of unit cid + (g >> 2) ncl.
+// (The plain loads and stores keep the DRAM stream full where the L2-side
+// adds of acc_tma 1 leave it idle part of the time.)
+struct OldBlocks {
+    float* buf;      // the warp's first buffer
+    uint32_t sbuf;   // its shared-memory address
+    uint32_t bars;   // the warp's first old_full barrier
+    int cid, ncl, num_units, q, half, rank;
+    int64_t m_rows;
+};
+
+// Coordinates (x = column, y = row) of block g; false past the warp's last tile.
+__device__ __forceinline__ bool old_block(const OldBlocks& L, const GemmArgs& a, uint32_t g, int32_t& x,
+                                          int32_t& y) {
+    const int t = L.cid + static_cast<int>(g >> 2) * L.ncl;
+    if (t >= L.num_units) return false;
+    int m, n;
+    tile_coords(t, a, m, n);
+    x = n * BN + 128 * L.half + 32 * static_cast<int>(g & 3);
+    y = (2 * m + L.rank) * BM + L.q * 32;
+    return true;
+}
+
+// Lane 0: the TMA load of block g's old values into its buffer, or for a
+// block past the accumulator's rows a plain arrival, so that every block
+// completes one phase of its buffer's barrier.
+__device__ __forceinline__ void old_issue(const OldBlocks& L, const GemmArgs& a, const CUtensorMap* map, uint32_t g) {
+    int32_t x, y;
+    if (!old_block(L, a, g, x, y)) return;
+    const uint32_t b = g % GRADW_PAIR_BUFS;
+    const uint32_t bar = L.bars + 8u * b;
+    if (y < L.m_rows && LCE_IN((x & 3) == 0 && x < a.N && y >= 0, a.status)) {
+        mbar_arrive_expect_tx(bar, EPI_STAGE_FLOATS * 4);
+        tma_load_2d(L.sbuf + b * EPI_STAGE_FLOATS * 4, map, bar, x, y);
+    } else {
+        mbar_arrive(bar);
+    }
+}
+
+// One tile of the read-modify-write (not inlined: the grad_W epilogue loop
+// stays within its registers); g: the warp's next block.  False if a
+// wait gave up (the caller drains the loads in flight).
+static __device__ __noinline__ bool gradw_tile_old(const GemmArgs& a, const OldBlocks& L, const CUtensorMap* map,
+                                               uint32_t& g, uint32_t taddr, int lane, uint32_t empty_bar,
+                                               SharedCtlPair* ctl, uint32_t peer_abort, uint64_t limit) {
+    const float s = ldexpf(*a.scale, -(P_SCALE_EXP + operand_scale_exp(*a.b_amax_bits)));
+    const int j0 = L.half * (BN / 64);
+    bool ok = true;
+#pragma unroll 1
+    for (int jj = 0; jj < BN / 64; ++jj, ++g) {
+        int32_t x = 0, y = 0;
+        old_block(L, a, g, x, y);
+        float v[32];
+        tmem_load_32cols(taddr + 32 * (j0 + jj), v);
+        const uint32_t b = g % GRADW_PAIR_BUFS;
+        if (!wait_phase_pair(L.bars + 8u * b, (g / GRADW_PAIR_BUFS) & 1u, ctl, peer_abort, a.status, limit)) {
+            ok = false;
+            break;
+        }
+        // the buffer is the TMA box's 128-byte-swizzled layout: row r's
+        // 16-byte slot k at slot k ^ (r & 7)
+        float* blk = L.buf + b * EPI_STAGE_FLOATS + lane * 32;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float4* p = reinterpret_cast<float4*>(blk + ((k ^ (lane & 7)) << 2));
+            float4 o = *p;
+            o.x = fmaf(s, v[4 * k], o.x);
+            o.y = fmaf(s, v[4 * k + 1], o.y);
+            o.z = fmaf(s, v[4 * k + 2], o.z);
+            o.w = fmaf(s, v[4 * k + 3], o.w);
+            *p = o;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            if (y < L.m_rows && LCE_IN((x & 3) == 0 && x < a.N && y >= 0, a.status)) {
+                tma_store_2d(map, L.sbuf + b * EPI_STAGE_FLOATS * 4, x, y);
+                bulk_commit_group();
+            }
+            bulk_wait_read_all();  // the store has read the buffer: the next load may fill it
+            old_issue(L, a, map, g + GRADW_PAIR_BUFS);
+        }
+        __syncwarp();
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) release_acc<true>(empty_bar);
+    return ok;
+}
+
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
@@ -70,9 +166,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle needs 1024-byte alignment
     // ring | grad_W block buffers (MODE_GRADW) | control block
-    constexpr int EPI_BYTES = MODE == MODE_GRADW ? EPI_STAGE_BYTES : 0;
+    constexpr int NST = pair_stages(MODE);
+    constexpr int EPI_BYTES = MODE == MODE_GRADW ? GRADW_PAIR_BUFS * EPI_STAGE_BYTES : 0;
     SharedCtlPair* ctl =
-        reinterpret_cast<SharedCtlPair*>(smem_raw + (base - raw) + PAIR_STAGES * PAIR_STAGE_BYTES + EPI_BYTES);
+        reinterpret_cast<SharedCtlPair*>(smem_raw + (base - raw) + NST * PAIR_STAGE_BYTES + EPI_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -80,14 +177,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
     // grad_W epilogue: this warp's block buffer (launched with the extra bytes)
-    float* const epi_stage = reinterpret_cast<float*>(smem_raw + (base - raw) + PAIR_STAGES * PAIR_STAGE_BYTES) +
-                             (warp >= 2 ? (warp - 2) * EPI_STAGE_FLOATS : 0);
+    float* const epi_stage = reinterpret_cast<float*>(smem_raw + (base - raw) + NST * PAIR_STAGE_BYTES) +
+                             (warp >= 2 ? (warp - 2) * GRADW_PAIR_BUFS * EPI_STAGE_FLOATS : 0);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < PAIR_STAGES; ++s) {
+        for (int s = 0; s < NST; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
             mbar_init(smem_u32(&ctl->empty[s]), 1);
         }
+        for (int w = 0; w < EPI_WARPS; ++w)
+            for (int b = 0; b < GRADW_PAIR_BUFS; ++b) mbar_init(smem_u32(&ctl->old_full[w][b]), 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctl->tmem_full[b]), 1);
             mbar_init(smem_u32(&ctl->tmem_empty[b]), 2 * EPI_WARPS);
@@ -168,13 +267,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                             tma_load_2d_pair(sb + j * 8192, &map_b, fb, bcol + 64 * j, args.b_y0 + k0);
                     }
                     ++issued;
-                    if (++stage == PAIR_STAGES) {
+                    if (++stage == NST) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            const uint64_t last = issued < PAIR_STAGES ? issued : PAIR_STAGES;
+            const uint64_t last = issued < NST ? issued : NST;
             if (!ok) {
                 // Let this CTA's copies still in flight land before it exits:
                 // rank 0 watches them on its barriers (which count both
@@ -183,8 +282,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 if (rank == 0) {
                     for (uint64_t i = 0; i < last; ++i) {
                         const uint64_t j = issued - 1 - i;
-                        wait_phase_pair(smem_u32(&ctl->full[j % PAIR_STAGES]),
-                                        static_cast<uint32_t>((j / PAIR_STAGES) & 1u), ctl, peer_abort, args.status,
+                        wait_phase_pair(smem_u32(&ctl->full[j % NST]),
+                                        static_cast<uint32_t>((j / NST) & 1u), ctl, peer_abort, args.status,
                                         limit, false);
                     }
                 } else {
@@ -197,8 +296,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 // arrive on this CTA's barriers, also from rank 0.
                 for (uint64_t i = 0; i < last; ++i) {
                     const uint64_t j = issued - 1 - i;
-                    if (!wait_phase_pair(smem_u32(&ctl->empty[j % PAIR_STAGES]),
-                                         static_cast<uint32_t>((j / PAIR_STAGES) & 1u), ctl, peer_abort,
+                    if (!wait_phase_pair(smem_u32(&ctl->empty[j % NST]),
+                                         static_cast<uint32_t>((j / NST) & 1u), ctl, peer_abort,
                                          args.status, limit, false))
                         break;
                 }
@@ -238,7 +337,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                         mma_f16kind_pair(d_tmem, adesc + A_STEP * k, bdesc + B_STEP * k, IDESC,
                                          (kb != kb0 || k != 0) ? 1u : 0u);
                     mma_commit_pair_multicast(smem_u32(&ctl->empty[stage]), 0x3);
-                    if (++stage == PAIR_STAGES) {
+                    if (++stage == NST) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -263,6 +362,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         if constexpr (MODE == MODE_LSE)
             side_init(args, side, static_cast<int64_t>(blockIdx.x) * EPI_WARPS + (warp - 2),
                       static_cast<int64_t>(gridDim.x) * EPI_WARPS, (num_tiles - cid + ncl - 1) / ncl);
+        // grad_W between the first and the last chunk (acc_tma 2): old blocks by TMA
+        const bool old_ldst = MODE == MODE_GRADW && args.acc_tma == 2 && !args.acc_first && !args.write_bf16;
+        OldBlocks ob;
+        uint32_t og = 0;  // the warp's next block
+        if (old_ldst) {
+            ob.buf = epi_stage;
+            ob.sbuf = smem_u32(epi_stage);
+            ob.bars = smem_u32(&ctl->old_full[warp - 2][0]);
+            ob.cid = cid;
+            ob.ncl = ncl;
+            ob.num_units = num_units;
+            ob.q = q;
+            ob.half = half;
+            ob.rank = static_cast<int>(rank);
+            ob.m_rows = m_rows;
+            if (lane == 0)
+                for (uint32_t g = 0; g < GRADW_PAIR_BUFS; ++g) old_issue(ob, args, &map_c, g);
+            __syncwarp();
+        }
+        bool old_ok = true;
         for (int t = cid; t < num_units; t += ncl) {
             int m, n, ks, kb0, kb1, tj;
             unit_coords(t, args, tp, k_blocks, m, n, ks, kb0, kb1, tj);
@@ -274,18 +393,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 if (gradw_reads_old(args) && c0 < args.N)
                     gradw_load_old(args, static_cast<int64_t>(mc) * BM + q * 32, m_rows, c0, lane, pre);
             }
-            if (!wait_phase_pair(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, peer_abort, args.status, limit))
+            if (!wait_phase_pair(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, peer_abort, args.status, limit)) {
+                old_ok = false;
                 break;
+            }
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            epilogue_tile<MODE, true>(args, mc, n, q, half, lane, taddr,
-                                      map_shared_rank(smem_u32(&ctl->tmem_empty[acc]), 0), m_rows, kb1 <= kb0, ks,
-                                      pre, epi_stage, &map_c, tj);
+            if (MODE == MODE_GRADW && old_ldst) {
+                if (!gradw_tile_old(args, ob, &map_c, og, taddr, lane,
+                                    map_shared_rank(smem_u32(&ctl->tmem_empty[acc]), 0), ctl, peer_abort, limit)) {
+                    old_ok = false;
+                    break;
+                }
+            } else {
+                epilogue_tile<MODE, true>(args, mc, n, q, half, lane, taddr,
+                                          map_shared_rank(smem_u32(&ctl->tmem_empty[acc]), 0), m_rows, kb1 <= kb0,
+                                          ks, pre, epi_stage, &map_c, tj);
+            }
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
             if constexpr (MODE == MODE_LSE) side_work(args, side, lane, side.budget);
         }
         if constexpr (MODE == MODE_LSE) side_work(args, side, lane, side.units);
+        // A wait that gave up (or an abort) leaves loads of old blocks in
+        // flight: let them land (bounded waits) before the CTA exits.
+        if (MODE == MODE_GRADW && old_ldst && !old_ok) {
+            for (uint32_t g = og; g < og + GRADW_PAIR_BUFS; ++g) {
+                int32_t x, y;
+                if (!old_block(ob, args, g, x, y)) break;
+                wait_phase_pair(ob.bars + 8u * (g % GRADW_PAIR_BUFS), (g / GRADW_PAIR_BUFS) & 1u, ctl, peer_abort,
+                                args.status, limit, false);
+            }
+        }
     }
 
     __syncwarp();  // reconverge the producer and MMA warps (one lane worked)

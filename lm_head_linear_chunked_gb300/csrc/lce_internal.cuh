@@ -44,7 +44,7 @@ constexpr int STAGES = 4;
 constexpr int A_STAGE_BYTES = BM * BK * 2;                 // 16 KB
 constexpr int B_STAGE_BYTES = BN * BK * 2;                 // 32 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES; // 48 KB
-constexpr int CTL_BYTES = 256;
+constexpr int CTL_BYTES = 512;
 constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + CTL_BYTES;
 // K-major B operands are loaded as boxes of 128 rows (two per 256-row tile
 // here; one per CTA in the pair form below).
@@ -69,10 +69,19 @@ constexpr int GEMM_PAIR_SMEM_BYTES = 1024 + PAIR_STAGES * PAIR_STAGE_BYTES + CTL
 // block; 1024-byte aligned, laid out as a 128-byte-swizzled TMA box).
 constexpr int EPI_STAGE_FLOATS = 32 * 32;
 constexpr int EPI_STAGE_BYTES = EPI_WARPS * EPI_STAGE_FLOATS * 4;  // 32 KB
+// In the pair form the grad_W epilogue has two such buffers per warp, so that
+// it can read the accumulator's old values a block ahead by TMA (acc_tma 2),
+// and its ring is one stage shorter to make room.
+constexpr int GRADW_PAIR_BUFS = 2;
+constexpr int PAIR_STAGES_GRADW = 5;
+constexpr int pair_stages(int mode) { return mode == MODE_GRADW ? PAIR_STAGES_GRADW : PAIR_STAGES; }
 constexpr int gemm_smem_bytes(int mode, bool pair) {
-    return (pair ? GEMM_PAIR_SMEM_BYTES : GEMM_SMEM_BYTES) + (mode == MODE_GRADW ? EPI_STAGE_BYTES : 0);
+    return pair ? 1024 + pair_stages(mode) * PAIR_STAGE_BYTES + CTL_BYTES +
+                      (mode == MODE_GRADW ? GRADW_PAIR_BUFS * EPI_STAGE_BYTES : 0)
+                : GEMM_SMEM_BYTES + (mode == MODE_GRADW ? EPI_STAGE_BYTES : 0);
 }
-static_assert(GEMM_SMEM_BYTES + EPI_STAGE_BYTES <= 232448 && GEMM_PAIR_SMEM_BYTES + EPI_STAGE_BYTES <= 232448,
+static_assert(gemm_smem_bytes(MODE_GRADW, false) <= 232448 && gemm_smem_bytes(MODE_GRADW, true) <= 232448 &&
+                  gemm_smem_bytes(MODE_LSE, true) <= 232448,
               "shared memory of one CTA");
 
 // grad_X's last partial wave (pair form).  Each grad_X tile runs the whole
@@ -214,7 +223,9 @@ struct GemmArgs {
     int32_t acc_first;   // MODE_GRADW: overwrite instead of accumulate
     int32_t write_bf16;  // MODE_GRADW: also write the bf16 cast
     int32_t acc_tma;     // MODE_GRADW: without write_bf16, store (first) or add (later) the tile into
-                         // out_f32 through the third tensor map (FP32 [M, N], 32x32 boxes, 128-byte swizzle)
+                         // out_f32 through the third tensor map (FP32 [M, N], 32x32 boxes, 128-byte swizzle):
+                         // 1: later chunks add at L2 (cp.reduce.async.bulk); 2 (pair form, N a multiple of
+                         // 256): later chunks load the old block by TMA, add in registers, store it by TMA
     // Valid-row compaction: the backward products skip ignored rows.
     //   MODE_LSE / MODE_G: row_map[chunk row] = row of the compacted P it is
     //     stored at (-1: ignored, not stored).
