@@ -88,7 +88,7 @@ typedef enum {
 } lce_status_t;
 
 /* Which entry point a workspace is sized for.  LCE_WS_FUSED is the size for
- * the fused call's fastest schedule: with chunks of at least 4096 rows, no
+ * the fused call's fastest schedule: with chunks of at least 256 rows, no
  * bias and two or more chunks, it holds two chunks of the kept fp16
  * exponentials, so that each chunk's forward also turns the previous
  * chunk's into the softmax while its tensor cores work.  LCE_WS_FUSED_MIN

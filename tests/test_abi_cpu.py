@@ -91,8 +91,8 @@ def test_workspace_sizes():
     fmin = lce.lce_workspace_size(N, H, V, 0, False, lce.WS_FUSED_MIN)
     assert fmin == fb - second and max(f, b) <= fmin <= f + b
     assert lce.lce_workspace_size(N, H, V, 0, True, lce.WS_FUSED_MIN) == with_bias
-    assert lce.lce_workspace_size(N, H, V, 2048, False, lce.WS_FUSED_MIN) == \
-        lce.lce_workspace_size(N, H, V, 2048, False, lce.WS_FUSED)  # chunks too small to overlap
+    assert lce.lce_workspace_size(N, H, V, 128, False, lce.WS_FUSED_MIN) == \
+        lce.lce_workspace_size(N, H, V, 128, False, lce.WS_FUSED)  # chunks too small to overlap
 
 
 @pytest.mark.parametrize("args,code", [
