@@ -549,6 +549,9 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             // pair form with whole 256-column tiles: later chunks read the old
             // accumulator blocks by TMA and store them back (plain streams)
             a.acc_tma = (form.pair && pb.H % BN == 0) ? 2 : 1;
+            // short K loops (chunks of up to 1024 rows): the tiles wait on the
+            // accumulator's traffic, so more of its reads in flight, fewer ring stages
+            a.gradw_bufs = a.k_blocks <= 16 ? 4 : 2;
             a.b_amax_bits = &hdr->amax_x_bits;
             a.dyn_rows = nvc + c;
             LCE_LAUNCH(PK_GRADW, launch_gemm(MODE_GRADW, mG_mn, mX16_mn, mAcc, a,

@@ -32,7 +32,7 @@ struct SharedCtlPair {
     uint64_t tmem_empty[2];
     uint64_t drain;
     uint64_t fin;
-    uint64_t old_full[EPI_WARPS][GRADW_PAIR_BUFS];  // grad_W (acc_tma 2): an old accumulator block has landed
+    uint64_t old_full[EPI_WARPS][GRADW_PAIR_BUFS_MAX];  // grad_W (acc_tma 2): an old accumulator block has landed
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -60,7 +60,7 @@ __device__ __forceinline__ bool wait_phase_pair(uint32_t bar, uint32_t parity, S
 
 // grad_W's read-modify-write of the FP32 accumulator in the chunks between
 // the first and the last (acc_tma 2).  Each epilogue warp streams its 32x32
-// blocks through its GRADW_PAIR_BUFS 4 KB buffers: the old values arrive by
+// blocks through its gradw_bufs 4 KB buffers: the old values arrive by
 // TMA load that many blocks ahead, the lanes add s times the accumulator in
 // place, and a TMA store writes the block back.  Block g of a warp is
 // 32-column slab g & 3 of its half of the tile of unit cid + (g >> 2) ncl.
@@ -70,6 +70,7 @@ struct OldBlocks {
     float* buf;      // the warp's first buffer
     uint32_t sbuf;   // its shared-memory address
     uint32_t bars;   // the warp's first old_full barrier
+    uint32_t nbuf, lg;  // buffers (2 or 4) and log2 of it
     int cid, ncl, num_units, q, half, rank;
     int64_t m_rows;
 };
@@ -92,7 +93,7 @@ __device__ __forceinline__ bool old_block(const OldBlocks& L, const GemmArgs& a,
 __device__ __forceinline__ void old_issue(const OldBlocks& L, const GemmArgs& a, const CUtensorMap* map, uint32_t g) {
     int32_t x, y;
     if (!old_block(L, a, g, x, y)) return;
-    const uint32_t b = g % GRADW_PAIR_BUFS;
+    const uint32_t b = g & (L.nbuf - 1);
     const uint32_t bar = L.bars + 8u * b;
     if (y < L.m_rows && LCE_IN((x & 3) == 0 && x < a.N && y >= 0, a.status)) {
         mbar_arrive_expect_tx(bar, EPI_STAGE_FLOATS * 4);
@@ -117,8 +118,8 @@ static __device__ __noinline__ bool gradw_tile_old(const GemmArgs& a, const OldB
         old_block(L, a, g, x, y);
         float v[32];
         tmem_load_32cols(taddr + 32 * (j0 + jj), v);
-        const uint32_t b = g % GRADW_PAIR_BUFS;
-        if (!wait_phase_pair(L.bars + 8u * b, (g / GRADW_PAIR_BUFS) & 1u, ctl, peer_abort, a.status, limit)) {
+        const uint32_t b = g & (L.nbuf - 1);
+        if (!wait_phase_pair(L.bars + 8u * b, (g >> L.lg) & 1u, ctl, peer_abort, a.status, limit)) {
             ok = false;
             break;
         }
@@ -143,7 +144,7 @@ static __device__ __noinline__ bool gradw_tile_old(const GemmArgs& a, const OldB
                 bulk_commit_group();
             }
             bulk_wait_read_all();  // the store has read the buffer: the next load may fill it
-            old_issue(L, a, map, g + GRADW_PAIR_BUFS);
+            old_issue(L, a, map, g + L.nbuf);
         }
         __syncwarp();
     }
@@ -166,10 +167,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle needs 1024-byte alignment
     // ring | grad_W block buffers (MODE_GRADW) | control block
-    constexpr int NST = pair_stages(MODE);
-    constexpr int EPI_BYTES = MODE == MODE_GRADW ? GRADW_PAIR_BUFS * EPI_STAGE_BYTES : 0;
-    SharedCtlPair* ctl =
-        reinterpret_cast<SharedCtlPair*>(smem_raw + (base - raw) + NST * PAIR_STAGE_BYTES + EPI_BYTES);
+    // grad_W: the 7 slots of 32 KB split into 7 - gradw_bufs ring stages and gradw_bufs epilogue buffers per warp
+    const int gbufs = (MODE == MODE_GRADW && args.gradw_bufs == 4) ? 4 : 2;
+    const int NST = MODE == MODE_GRADW ? GRADW_PAIR_SLOTS - gbufs : PAIR_STAGES;
+    constexpr int SLOTS = MODE == MODE_GRADW ? GRADW_PAIR_SLOTS : PAIR_STAGES;
+    SharedCtlPair* ctl = reinterpret_cast<SharedCtlPair*>(smem_raw + (base - raw) + SLOTS * PAIR_STAGE_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -178,7 +180,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t peer = rank ^ 1u;
     // grad_W epilogue: this warp's block buffer (launched with the extra bytes)
     float* const epi_stage = reinterpret_cast<float*>(smem_raw + (base - raw) + NST * PAIR_STAGE_BYTES) +
-                             (warp >= 2 ? (warp - 2) * GRADW_PAIR_BUFS * EPI_STAGE_FLOATS : 0);
+                             (warp >= 2 ? (warp - 2) * gbufs * EPI_STAGE_FLOATS : 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
@@ -186,7 +188,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             mbar_init(smem_u32(&ctl->empty[s]), 1);
         }
         for (int w = 0; w < EPI_WARPS; ++w)
-            for (int b = 0; b < GRADW_PAIR_BUFS; ++b) mbar_init(smem_u32(&ctl->old_full[w][b]), 1);
+            for (int b = 0; b < GRADW_PAIR_BUFS_MAX; ++b) mbar_init(smem_u32(&ctl->old_full[w][b]), 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctl->tmem_full[b]), 1);
             mbar_init(smem_u32(&ctl->tmem_empty[b]), 2 * EPI_WARPS);
@@ -273,7 +275,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     }
                 }
             }
-            const uint64_t last = issued < NST ? issued : NST;
+            const uint64_t last = issued < static_cast<uint64_t>(NST) ? issued : static_cast<uint64_t>(NST);
             if (!ok) {
                 // Let this CTA's copies still in flight land before it exits:
                 // rank 0 watches them on its barriers (which count both
@@ -370,6 +372,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             ob.buf = epi_stage;
             ob.sbuf = smem_u32(epi_stage);
             ob.bars = smem_u32(&ctl->old_full[warp - 2][0]);
+            ob.nbuf = static_cast<uint32_t>(gbufs);
+            ob.lg = gbufs == 4 ? 2u : 1u;
             ob.cid = cid;
             ob.ncl = ncl;
             ob.num_units = num_units;
@@ -378,7 +382,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             ob.rank = static_cast<int>(rank);
             ob.m_rows = m_rows;
             if (lane == 0)
-                for (uint32_t g = 0; g < GRADW_PAIR_BUFS; ++g) old_issue(ob, args, &map_c, g);
+                for (uint32_t g = 0; g < ob.nbuf; ++g) old_issue(ob, args, &map_c, g);
             __syncwarp();
         }
         bool old_ok = true;
@@ -418,10 +422,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         // A wait that gave up (or an abort) leaves loads of old blocks in
         // flight: let them land (bounded waits) before the CTA exits.
         if (MODE == MODE_GRADW && old_ldst && !old_ok) {
-            for (uint32_t g = og; g < og + GRADW_PAIR_BUFS; ++g) {
+            for (uint32_t g = og; g < og + ob.nbuf; ++g) {
                 int32_t x, y;
                 if (!old_block(ob, args, g, x, y)) break;
-                wait_phase_pair(ob.bars + 8u * (g % GRADW_PAIR_BUFS), (g / GRADW_PAIR_BUFS) & 1u, ctl, peer_abort,
+                wait_phase_pair(ob.bars + 8u * (g & (ob.nbuf - 1)), (g >> ob.lg) & 1u, ctl, peer_abort,
                                 args.status, limit, false);
             }
         }

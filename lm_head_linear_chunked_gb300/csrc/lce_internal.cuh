@@ -69,17 +69,18 @@ constexpr int GEMM_PAIR_SMEM_BYTES = 1024 + PAIR_STAGES * PAIR_STAGE_BYTES + CTL
 // block; 1024-byte aligned, laid out as a 128-byte-swizzled TMA box).
 constexpr int EPI_STAGE_FLOATS = 32 * 32;
 constexpr int EPI_STAGE_BYTES = EPI_WARPS * EPI_STAGE_FLOATS * 4;  // 32 KB
-// In the pair form the grad_W epilogue has two such buffers per warp, so that
-// it can read the accumulator's old values a block ahead by TMA (acc_tma 2),
-// and its ring is one stage shorter to make room.
-constexpr int GRADW_PAIR_BUFS = 2;
-constexpr int PAIR_STAGES_GRADW = 5;
-constexpr int pair_stages(int mode) { return mode == MODE_GRADW ? PAIR_STAGES_GRADW : PAIR_STAGES; }
+// In the pair form the grad_W kernel shares 7 x 32 KB between its ring and
+// its epilogue buffers (GemmArgs::gradw_bufs per warp, 2 or 4, so that it can
+// read the accumulator's old values that many blocks ahead by TMA; acc_tma 2):
+// 5 ring stages and 2 buffers per warp for long K loops, 3 and 4 for short
+// ones, whose tiles wait on the accumulator's traffic rather than the MMAs.
+constexpr int GRADW_PAIR_SLOTS = 7;
+constexpr int GRADW_PAIR_BUFS_MAX = 4;
 constexpr int gemm_smem_bytes(int mode, bool pair) {
-    return pair ? 1024 + pair_stages(mode) * PAIR_STAGE_BYTES + CTL_BYTES +
-                      (mode == MODE_GRADW ? GRADW_PAIR_BUFS * EPI_STAGE_BYTES : 0)
+    return pair ? 1024 + (mode == MODE_GRADW ? GRADW_PAIR_SLOTS : PAIR_STAGES) * PAIR_STAGE_BYTES + CTL_BYTES
                 : GEMM_SMEM_BYTES + (mode == MODE_GRADW ? EPI_STAGE_BYTES : 0);
 }
+static_assert(PAIR_STAGE_BYTES == EPI_STAGE_BYTES, "a ring stage and a set of epilogue buffers take the same bytes");
 static_assert(gemm_smem_bytes(MODE_GRADW, false) <= 232448 && gemm_smem_bytes(MODE_GRADW, true) <= 232448 &&
                   gemm_smem_bytes(MODE_LSE, true) <= 232448,
               "shared memory of one CTA");
@@ -222,6 +223,7 @@ struct GemmArgs {
     int64_t ld_f32;
     int32_t acc_first;   // MODE_GRADW: overwrite instead of accumulate
     int32_t write_bf16;  // MODE_GRADW: also write the bf16 cast
+    int32_t gradw_bufs;  // MODE_GRADW, pair form: epilogue buffers per warp (2 or 4; the ring gets 7 - this stages)
     int32_t acc_tma;     // MODE_GRADW: without write_bf16, store (first) or add (later) the tile into
                          // out_f32 through the third tensor map (FP32 [M, N], 32x32 boxes, 128-byte swizzle):
                          // 1: later chunks add at L2 (cp.reduce.async.bulk); 2 (pair form, N a multiple of
