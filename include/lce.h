@@ -236,12 +236,13 @@ LCE_API const char* lce_status_string(lce_status_t status);
  * ends with an error status instead of a hang.
  *
  * lce_debug_gradx_tail_plan: how the pair form splits the last partial
- * round of a grad_X launch over K.  For `tiles` output tiles of 256 x 256
- * with valid rows, `slots` pairs and a K extent of `k_blocks` blocks of 64,
- * writes out[0] = tiles computed whole, out[1] = tiles split after them
- * (0: no split), out[2] = K slices per split tile, out[3] = k-blocks per
- * slice.  Host-only; returns LCE_ERR_INVALID_ARG for a null `out` or a
- * negative or out-of-range count. */
+ * round of a grad_X launch over K.  For `tiles` output tiles of 256 rows x
+ * `tile_cols` columns (256, or 512 where H is a multiple of 512) with valid
+ * rows, `slots` pairs and a K extent of `k_blocks` blocks of 64, writes
+ * out[0] = tiles computed whole, out[1] = tiles split after them (0: no
+ * split), out[2] = K slices per split tile, out[3] = k-blocks per slice.
+ * Host-only; returns LCE_ERR_INVALID_ARG for a null `out`, a negative or
+ * out-of-range count, or another tile width. */
 LCE_API lce_status_t lce_debug_gemm(int layout, int64_t M, int64_t N, int64_t K,
                             const lce_bf16* A, const lce_bf16* B, float* D,
                             void* ws, size_t ws_bytes, lce_stream_t stream);
@@ -250,7 +251,7 @@ LCE_API lce_status_t lce_debug_wait_timeout(uint32_t limit_us, void* ws, size_t 
                                     lce_stream_t stream);
 
 LCE_API lce_status_t lce_debug_gradx_tail_plan(int64_t tiles, int64_t slots, int64_t k_blocks,
-                                       int64_t out[4]);
+                                       int64_t tile_cols, int64_t out[4]);
 
 /* lce_forward without a caller-provided workspace, for callers that cannot
  * allocate device memory: for example a hook running inside a framework

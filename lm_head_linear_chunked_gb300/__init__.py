@@ -67,7 +67,7 @@ _SIGS = {
     "lce_status_string": [_STATUS],
     "lce_debug_gemm": [ctypes.c_int, _I64, _I64, _I64, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "lce_debug_wait_timeout": [ctypes.c_uint32, _P, ctypes.c_size_t, _P],
-    "lce_debug_gradx_tail_plan": [_I64, _I64, _I64, ctypes.POINTER(_I64)],
+    "lce_debug_gradx_tail_plan": [_I64, _I64, _I64, _I64, ctypes.POINTER(_I64)],
     "lce_forward_static_ws": [_I64, _I64, _I64, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _P],
     "lce_static_ws_check_status": [_P],
     "lce_scale_grads": [_I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P],
@@ -242,11 +242,12 @@ def lce_debug_wait_timeout(limit_us, ws, ws_bytes, stream) -> None:
     _check(lib().lce_debug_wait_timeout(limit_us, _ptr(ws), ws_bytes, _stream(stream)), "lce_debug_wait_timeout")
 
 
-def lce_debug_gradx_tail_plan(tiles, slots, k_blocks) -> tuple:
+def lce_debug_gradx_tail_plan(tiles, slots, k_blocks, tile_cols=256) -> tuple:
     """(tiles computed whole, tiles split over K after them, slices per split
-    tile, k-blocks per slice) of a pair-form grad_X launch."""
+    tile, k-blocks per slice) of a pair-form grad_X launch whose tiles are
+    256 rows x tile_cols (256 or 512) columns."""
     out = (_I64 * 4)()
-    _check(lib().lce_debug_gradx_tail_plan(tiles, slots, k_blocks, out), "lce_debug_gradx_tail_plan")
+    _check(lib().lce_debug_gradx_tail_plan(tiles, slots, k_blocks, tile_cols, out), "lce_debug_gradx_tail_plan")
     return tuple(int(v) for v in out)
 
 

@@ -487,9 +487,12 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             !map_16bit_2d(&mX16_mn, X16, rows, pb.H, pb.H, 64, 64, true))
             return LCE_ERR_CUDA;
         if (o.grad_X) {   // grad_X_c = s (P W - W[y])
+            // pair form with the tail split and H a multiple of 512: 256 x 512 tiles
+            const bool wide = tail != nullptr && pb.H % (2 * BN) == 0;
+            const int nw = wide ? 2 : 1;
             GemmArgs a = call_args();
             a.m_tiles = static_cast<int32_t>(mtf);
-            a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN));
+            a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN * nw));
             a.k_blocks = static_cast<int32_t>(cdiv(pb.V, BK));
             // pair form: H tiles fastest, so that each wave covers whole rows of
             // grad_X and every tile sharing a P row block runs at once (measured:
@@ -515,14 +518,15 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             a.split_out = split_out;
             a.split_stride = p.C * pb.H;
             a.tail_out = tail;
-            a.tail_units_max = TAIL_UNITS_MAX;
+            a.tail_units_max = TAIL_UNITS_MAX / nw;
             // with the tail split, a chunk of fewer tiles than pairs still gets every
             // pair: its slices spread over them
             const int grid = grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles *
                                                (tail ? TAIL_SPLIT_MAX : p.gradx_splits));
-            LCE_LAUNCH(PK_GRADX, launch_gemm(MODE_GRADX, mG_k, mW16_mn, mW16_mn, a, grid, s, form.pair));
+            LCE_LAUNCH(PK_GRADX, launch_gemm(wide ? MODE_GRADX_W : MODE_GRADX, mG_k, mW16_mn, mW16_mn, a, grid, s,
+                                             form.pair));
             if (tail)  // the same plan as the GEMM's: its pairs, tile columns and K extent
-                LCE_LAUNCH(PK_GRADX, launch_gradx_tail_reduce(tail, grid / 2, a.n_tiles, a.k_blocks, pb.H, crow + r0,
+                LCE_LAUNCH(PK_GRADX, launch_gradx_tail_reduce(tail, grid / 2, a.n_tiles, a.k_blocks, nw, pb.H, crow + r0,
                                                               nvc + c, rows, pb.y + r0, pb.ignore_index, pb.V, pb.W,
                                                               tcoef + r0, hdr, o.grad_X + r0 * pb.H, s));
             if (split_out)
@@ -610,6 +614,7 @@ cudaError_t launch_gemm(int mode, const CUtensorMap& map_a, const CUtensorMap& m
         case MODE_G: return launch_gemm_logits(mode, map_a, map_b, map_c, args, grid, stream, pair);
         case MODE_GRADX:
         case MODE_GRADW: return launch_gemm_grads(mode, map_a, map_b, map_c, args, grid, stream, pair);
+        case MODE_GRADX_W: return launch_gemm_gradx_wide(map_a, map_b, map_c, args, grid, stream, pair);
         default: return launch_gemm_plain(mode, map_a, map_b, map_c, args, grid, stream, pair);
     }
 }
@@ -827,12 +832,13 @@ int lce_set_gemm_form(int form) {
     return g_gemm_form.exchange(form);
 }
 
-lce_status_t lce_debug_gradx_tail_plan(int64_t tiles, int64_t slots, int64_t k_blocks, int64_t out[4]) {
+lce_status_t lce_debug_gradx_tail_plan(int64_t tiles, int64_t slots, int64_t k_blocks, int64_t tile_cols,
+                                       int64_t out[4]) {
     if (!out || tiles < 0 || slots < 0 || k_blocks < 0 || tiles > INT32_MAX || slots > INT32_MAX ||
-        k_blocks > INT32_MAX)
+        k_blocks > INT32_MAX || (tile_cols != BN && tile_cols != 2 * BN))
         return LCE_ERR_INVALID_ARG;
-    const TailPlan tp =
-        gradx_tail_plan(static_cast<int>(tiles), static_cast<int>(slots), static_cast<int>(k_blocks));
+    const TailPlan tp = gradx_tail_plan(static_cast<int>(tiles), static_cast<int>(slots), static_cast<int>(k_blocks),
+                                        static_cast<int>(TAIL_UNITS_MAX / (tile_cols / BN)));
     out[0] = tp.full;
     out[1] = tp.tail;
     out[2] = tp.s;

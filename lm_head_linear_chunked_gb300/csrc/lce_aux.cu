@@ -646,22 +646,25 @@ __global__ void gradx_split_reduce_kernel(const float* __restrict__ split_out, i
 // plan is recomputed from the chunk's valid rows as the GEMM computed it;
 // for each tail tile's valid row and column, the slices' partial tiles are
 // summed in slice order, then finished as the unsplit epilogue does.  One
-// thread per 8 columns of a row, consecutive threads along the row.
+// thread per 8 columns of a row, consecutive threads along the row.  nw: the
+// tiles' width in 256-column pieces (1 or 2).
 __global__ void gradx_tail_reduce_kernel(const float* __restrict__ tail_out, int slots, int n_tiles, int k_blocks,
-                                         int64_t H, const int* __restrict__ crow, const int* __restrict__ n_valid,
-                                         const int64_t* __restrict__ y, int64_t ignore_index, int64_t V,
-                                         const uint16_t* __restrict__ W, const float* __restrict__ tcoef,
-                                         const WsHeader* hdr, uint16_t* __restrict__ grad_X_chunk,
-                                         int64_t max_rows) {
+                                         int nw, int64_t H, const int* __restrict__ crow,
+                                         const int* __restrict__ n_valid, const int64_t* __restrict__ y,
+                                         int64_t ignore_index, int64_t V, const uint16_t* __restrict__ W,
+                                         const float* __restrict__ tcoef, const WsHeader* hdr,
+                                         uint16_t* __restrict__ grad_X_chunk, int64_t max_rows) {
     const int64_t nv = *n_valid;
+    const int max_units = TAIL_UNITS_MAX / nw;
     const TailPlan tp =
-        gradx_tail_plan(static_cast<int>((nv + 2 * BM - 1) / (2 * BM)) * n_tiles, slots, k_blocks);
+        gradx_tail_plan(static_cast<int>((nv + 2 * BM - 1) / (2 * BM)) * n_tiles, slots, k_blocks, max_units);
     if (tp.tail == 0) return;
-    if (!LCE_IN(static_cast<int64_t>(tp.tail) * tp.s <= TAIL_UNITS_MAX, const_cast<unsigned*>(&hdr->status)))
-        return;
+    if (!LCE_IN(tp.tail * tp.s <= max_units, const_cast<unsigned*>(&hdr->status))) return;
     const float s = hdr->scale;
     const float f = ldexpf(s, -(P_SCALE_EXP + operand_scale_exp(hdr->amax_w_bits)));
-    constexpr int G = BN / 8;  // 8-column groups per tile row
+    const int tw = BN * nw;         // tile width
+    const int G = tw / 8;           // 8-column groups per tile row
+    const int64_t tile_floats = TAIL_TILE_FLOATS * nw;
     const int64_t total = static_cast<int64_t>(tp.tail) * (2 * BM) * G;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total; e += stride) {
@@ -670,13 +673,14 @@ __global__ void gradx_tail_reduce_kernel(const float* __restrict__ tail_out, int
         const int tr = rem / G, g = rem - tr * G;
         const int t = tp.full + i;  // tile order n fastest: tile t is (t / n_tiles, t % n_tiles)
         const int64_t j = static_cast<int64_t>(t / n_tiles) * (2 * BM) + tr;
-        const int64_t h = static_cast<int64_t>(t % n_tiles) * BN + 8 * g;
+        const int64_t h = static_cast<int64_t>(t % n_tiles) * tw + 8 * g;
         if (j >= nv || h >= H) continue;
         float sum[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) sum[k] = 0.f;
         for (int ks = 0; ks < tp.s; ++ks)
-            add8(sum, tail_out + (static_cast<int64_t>(ks) * tp.tail + i) * TAIL_TILE_FLOATS + tr * BN + 8 * g);
+            add8(sum, tail_out + (static_cast<int64_t>(ks) * tp.tail + i) * tile_floats + static_cast<int64_t>(tr) * tw +
+                          8 * g);
         gradx_finish8(sum, j, h, H, s, f, crow, y, ignore_index, V, W, tcoef, hdr, grad_X_chunk, max_rows);
     }
 }
@@ -888,14 +892,15 @@ cudaError_t launch_scale_grads(int64_t N, int64_t H, int64_t V, const float* d_g
     return cudaGetLastError();
 }
 
-cudaError_t launch_gradx_tail_reduce(const float* tail_out, int slots, int n_tiles, int k_blocks, int64_t H,
+cudaError_t launch_gradx_tail_reduce(const float* tail_out, int slots, int n_tiles, int k_blocks, int nw, int64_t H,
                                      const int* crow, const int* n_valid, int64_t max_rows, const int64_t* y,
                                      int64_t ignore_index, int64_t V, const uint16_t* W, const float* tcoef,
                                      const WsHeader* hdr, uint16_t* grad_X_chunk, cudaStream_t s) {
-    // at most slots - 1 tail tiles of 256 rows x 32 groups of 8 columns
-    const int64_t want = (static_cast<int64_t>(slots) * 2 * BM * (BN / 8) + 255) / 256;
+    if (nw != 1 && nw != 2) return cudaErrorInvalidValue;
+    // at most slots - 1 tail tiles of 256 rows x (32 nw) groups of 8 columns
+    const int64_t want = (static_cast<int64_t>(slots) * 2 * BM * (BN * nw / 8) + 255) / 256;
     const int blocks = static_cast<int>(want < 1 ? 1 : (want < 1216 ? want : 1216));
-    gradx_tail_reduce_kernel<<<blocks, 256, 0, s>>>(tail_out, slots, n_tiles, k_blocks, H, crow, n_valid, y,
+    gradx_tail_reduce_kernel<<<blocks, 256, 0, s>>>(tail_out, slots, n_tiles, k_blocks, nw, H, crow, n_valid, y,
                                                     ignore_index, V, W, tcoef, hdr, grad_X_chunk, max_rows);
     return cudaGetLastError();
 }

@@ -35,9 +35,10 @@ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? 
 template <int MODE>
 struct ModeTraits {
     static constexpr bool A_MN = (MODE == MODE_PLAIN_MM || MODE == MODE_GRADW);
-    static constexpr bool B_MN = (MODE == MODE_PLAIN_KM || MODE == MODE_PLAIN_MM ||
-                                  MODE == MODE_GRADX || MODE == MODE_GRADW);
-    static constexpr bool F16 = (MODE == MODE_GRADX || MODE == MODE_GRADW);
+    static constexpr bool B_MN = (MODE == MODE_PLAIN_KM || MODE == MODE_PLAIN_MM || is_gradx(MODE) ||
+                                  MODE == MODE_GRADW);
+    static constexpr bool F16 = (is_gradx(MODE) || MODE == MODE_GRADW);
+    static constexpr int NW = MODE == MODE_GRADX_W ? 2 : 1;  // output tile width in 256-column MMAs
 };
 
 struct SharedCtl {
@@ -330,9 +331,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
                                               uint32_t taddr, uint32_t empty_bar, int64_t m_rows,
                                               bool zero_acc, int ks, const float4 (&pre)[8], float* stage,
                                               const CUtensorMap* map_c, int tj = -1) {
+    constexpr int TW = BN * ModeTraits<MODE>::NW;  // output tile width
     const int64_t row = static_cast<int64_t>(m) * BM + q * 32 + lane;
-    const int64_t col0 = static_cast<int64_t>(n) * BN;
-    const int j0 = half * (BN / 64);  // this warp's four 32-column chunks: half of the tile's columns
+    const int64_t col0 = static_cast<int64_t>(n) * TW;
+    const int j0 = half * (TW / 64);  // this warp's 32-column chunks: half of the tile's columns
     const bool row_ok = row < m_rows;
     // MODE_LSE / MODE_G: where this row's E or P row goes (-1: not stored)
     const int64_t prow = (a.row_map && row_ok) ? static_cast<int64_t>(a.row_map[row]) : (row_ok ? row : -1);
@@ -350,7 +352,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         float mz = -INFINITY, zt = 0.f;
         bool got = false;
 #pragma unroll 1
-        for (int j = j0; j < j0 + BN / 64; ++j) {
+        for (int j = j0; j < j0 + TW / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
             if (c0 >= a.N) break;
             float v[32];
@@ -376,7 +378,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         const float mx = mz * LOG2E_F;
         float sm = 0.f;
 #pragma unroll 1
-        for (int j = j0; j < j0 + BN / 64; ++j) {
+        for (int j = j0; j < j0 + TW / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
             if (c0 >= a.N) break;
             float v[32];
@@ -421,7 +423,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         const float lse2 = row_ok ? a.lse[row] * LOG2E_F : 0.f;
         float se = 0.f;
 #pragma unroll 1
-        for (int j = j0; j < j0 + BN / 64; ++j) {
+        for (int j = j0; j < j0 + TW / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
             if (c0 >= a.N) break;
             float v[32];
@@ -453,7 +455,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         if (lane == 0) release_acc<PAIR>(empty_bar);
         if (row_ok && a.part_s && LCE_IN(2 * n + half < a.cap_pt && row < a.ldp, a.status))
             a.part_s[(2 * static_cast<int64_t>(n) + half) * a.ldp + row] = se;
-    } else if constexpr (MODE == MODE_GRADX) {
+    } else if constexpr (is_gradx(MODE)) {
       if (a.k_splits > 1 || tj >= 0) {
         // one K slice of a split product: the raw fp32 partial sums, finished
         // by a reduction kernel (fixed slice order).  A split tail unit's
@@ -461,7 +463,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         // this column), the k_splits form's to the slice's rows of the chunk.
         const bool tail = tj >= 0;
         const int64_t trow = row - static_cast<int64_t>(m >> 1) * (2 * BM);  // row within the pair tile
-        float* dst = tail ? a.tail_out + static_cast<int64_t>(tj) * TAIL_TILE_FLOATS + trow * BN
+        float* dst = tail ? a.tail_out + static_cast<int64_t>(tj) * (TAIL_TILE_FLOATS * ModeTraits<MODE>::NW) +
+                                trow * TW
                           : a.split_out + static_cast<int64_t>(ks) * a.split_stride + row * a.N;
         const int64_t cbase = tail ? col0 : 0;  // dst's first column
         // rows past the valid ones are not stored (and not checked)
@@ -469,7 +472,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
                                                     a.status)
                                            : LCE_IN(ks < a.k_splits && row < a.cap_rows, a.status));
 #pragma unroll 1
-        for (int j = j0; j < j0 + BN / 64; ++j) {
+        for (int j = j0; j < j0 + TW / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
             if (c0 >= a.N) break;
             float v[32];
@@ -496,7 +499,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         const float sc = valid ? s * a.tcoef[orow] : 0.f;
         const uint16_t* wy = a.w_rows + (valid ? yr : 0) * a.ldw;
 #pragma unroll 1
-        for (int j = j0; j < j0 + BN / 64; ++j) {
+        for (int j = j0; j < j0 + TW / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
             if (c0 >= a.N) break;
             float v[32];
@@ -621,7 +624,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, int m, int n, i
         if (lane == 0) release_acc<PAIR>(empty_bar);
     } else {  // PLAIN: D = fp32 product
 #pragma unroll 1
-        for (int j = j0; j < j0 + BN / 64; ++j) {
+        for (int j = j0; j < j0 + TW / 64; ++j) {
             const int64_t c0 = col0 + 32 * j;
             if (c0 >= a.N) break;
             float v[32];

@@ -169,9 +169,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     // ring | grad_W block buffers (MODE_GRADW) | control block
     // grad_W: the 7 slots of 32 KB split into 7 - gradw_bufs ring stages and gradw_bufs epilogue buffers per warp
     const int gbufs = (MODE == MODE_GRADW && args.gradw_bufs == 4) ? 4 : 2;
-    const int NST = MODE == MODE_GRADW ? GRADW_PAIR_SLOTS - gbufs : PAIR_STAGES;
-    constexpr int SLOTS = MODE == MODE_GRADW ? GRADW_PAIR_SLOTS : PAIR_STAGES;
-    SharedCtlPair* ctl = reinterpret_cast<SharedCtlPair*>(smem_raw + (base - raw) + SLOTS * PAIR_STAGE_BYTES);
+    const int NST = MODE == MODE_GRADW ? GRADW_PAIR_SLOTS - gbufs : (MODE == MODE_GRADX_W ? GRADX_W_STAGES : PAIR_STAGES);
+    constexpr int NW = T::NW;                     // 256-column MMAs per output tile
+    constexpr int SB = pair_stage_bytes(MODE);    // bytes of one K slice in this CTA
+    SharedCtlPair* ctl = reinterpret_cast<SharedCtlPair*>(smem_raw + (base - raw) + pair_ring_bytes(MODE));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -217,14 +218,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const int cid = static_cast<int>(blockIdx.x >> 1);
     const int ncl = static_cast<int>(gridDim.x >> 1);
     const int dyn = args.dyn_rows ? *args.dyn_rows : -1;
-    const int64_t m_rows = (MODE == MODE_GRADX && dyn >= 0) ? static_cast<int64_t>(dyn) : args.M;
+    const int64_t m_rows = (is_gradx(MODE) && dyn >= 0) ? static_cast<int64_t>(dyn) : args.M;
     const int k_blocks = (MODE == MODE_GRADW && dyn >= 0) ? (dyn + BK - 1) / BK : args.k_blocks;
     // grad_X: the last partial round of tiles split over K.  With n fastest in
     // the tile order, the tiles that hold valid rows are the first ones.
     TailPlan tp{num_tiles, 0, 1, k_blocks};
     int num_units = num_tiles;
-    if (MODE == MODE_GRADX && args.tail_out && args.k_splits <= 1 && args.raster == 1) {
-        tp = gradx_tail_plan(static_cast<int>((m_rows + PAIR_BM - 1) / PAIR_BM) * args.n_tiles, ncl, k_blocks);
+    if (is_gradx(MODE) && args.tail_out && args.k_splits <= 1 && args.raster == 1) {
+        tp = gradx_tail_plan(static_cast<int>((m_rows + PAIR_BM - 1) / PAIR_BM) * args.n_tiles, ncl, k_blocks,
+                             TAIL_UNITS_MAX / NW);
         num_units = tp.full + tp.tail * tp.s;
     }
 
@@ -239,7 +241,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 unit_coords(t, args, tp, k_blocks, m, n, ks, kb0, kb1, tj);
                 if (static_cast<int64_t>(m) * PAIR_BM >= m_rows) continue;
                 const int32_t arow = m * PAIR_BM + static_cast<int32_t>(rank) * BM;
-                const int32_t bcol = n * BN + static_cast<int32_t>(rank) * (BN / 2);
+                // this CTA's half of each 256-column piece of the tile's B
+                const int32_t bcol = n * (BN * NW) + static_cast<int32_t>(rank) * (BN / 2);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase_pair(smem_u32(&ctl->empty[stage]), phase ^ 1u, ctl, peer_abort, args.status,
                                          limit)) {
@@ -248,8 +251,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     }
                     // rank 0's barrier counts both CTAs' bytes of the slice
                     const uint32_t fb = map_shared_rank(smem_u32(&ctl->full[stage]), 0);
-                    if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[stage]), 2 * PAIR_STAGE_BYTES);
-                    const uint32_t sa = base + stage * PAIR_STAGE_BYTES;
+                    if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[stage]), 2 * SB);
+                    const uint32_t sa = base + stage * SB;
                     const uint32_t sb = sa + A_STAGE_BYTES;
                     const int32_t k0 = kb * BK;
                     // innermost coordinates: multiples of 8 16-bit elements (16 bytes)
@@ -265,8 +268,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                         tma_load_2d_pair(sb, &map_b, fb, k0, args.b_y0 + bcol);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < (BN / 2) / 64; ++j)
-                            tma_load_2d_pair(sb + j * 8192, &map_b, fb, bcol + 64 * j, args.b_y0 + k0);
+                        for (int p = 0; p < NW; ++p)
+#pragma unroll
+                            for (int j = 0; j < (BN / 2) / 64; ++j)
+                                tma_load_2d_pair(sb + p * PAIR_B_STAGE_BYTES + j * 8192, &map_b, fb,
+                                                 bcol + p * BN + 64 * j, args.b_y0 + k0);
                     }
                     ++issued;
                     if (++stage == NST) {
@@ -323,21 +329,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + acc * BN;
+                const uint32_t d_tmem = tmem_base + acc * BN;  // (acc stays 0 with 512-column tiles)
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase_pair(smem_u32(&ctl->full[stage]), phase, ctl, peer_abort, args.status, limit)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t sa = base + stage * PAIR_STAGE_BYTES;
+                    const uint32_t sa = base + stage * SB;
                     const uint32_t sb = sa + A_STAGE_BYTES;
                     const uint64_t adesc = T::A_MN ? smem_desc_sw128(sa, 8192, 1024) : smem_desc_sw128(sa, 16, 1024);
-                    const uint64_t bdesc = T::B_MN ? smem_desc_sw128(sb, 8192, 1024) : smem_desc_sw128(sb, 16, 1024);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        mma_f16kind_pair(d_tmem, adesc + A_STEP * k, bdesc + B_STEP * k, IDESC,
-                                         (kb != kb0 || k != 0) ? 1u : 0u);
+                    for (int p = 0; p < NW; ++p) {  // piece p: output columns 256 p .. 256 p + 255
+                        const uint32_t sbp = sb + p * PAIR_B_STAGE_BYTES;
+                        const uint64_t bdesc =
+                            T::B_MN ? smem_desc_sw128(sbp, 8192, 1024) : smem_desc_sw128(sbp, 16, 1024);
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k)
+                            mma_f16kind_pair(d_tmem + p * BN, adesc + A_STEP * k, bdesc + B_STEP * k, IDESC,
+                                             (kb != kb0 || k != 0) ? 1u : 0u);
+                    }
                     mma_commit_pair_multicast(smem_u32(&ctl->empty[stage]), 0x3);
                     if (++stage == NST) {
                         stage = 0;
@@ -346,7 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 }
                 if (!ok) break;
                 mma_commit_pair_multicast(smem_u32(&ctl->tmem_full[acc]), 0x3);
-                acc ^= 1u;
+                if (NW == 1) acc ^= 1u;  // two accumulators of 256 columns, or one of 512
                 if (acc == 0) acc_phase ^= 1u;
             }
             if (!ok) {
@@ -414,7 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                                           map_shared_rank(smem_u32(&ctl->tmem_empty[acc]), 0), m_rows, kb1 <= kb0,
                                           ks, pre, epi_stage, &map_c, tj);
             }
-            acc ^= 1u;
+            if (NW == 1) acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
             if constexpr (MODE == MODE_LSE) side_work(args, side, lane, side.budget);
         }
@@ -468,8 +479,12 @@ cudaError_t launch_gemm_pair(const CUtensorMap& map_a, const CUtensorMap& map_b,
 template <int MODE>
 cudaError_t launch_gemm_mode(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_c,
                              const GemmArgs& args, int grid, cudaStream_t stream, bool pair) {
-    return pair ? launch_gemm_pair<MODE>(map_a, map_b, map_c, args, grid, stream)
-                : launch_gemm_single<MODE>(map_a, map_b, map_c, args, grid, stream);
+    if constexpr (MODE == MODE_GRADX_W) {  // 512-column tiles exist in the pair form only
+        return pair ? launch_gemm_pair<MODE>(map_a, map_b, map_c, args, grid, stream) : cudaErrorInvalidValue;
+    } else {
+        return pair ? launch_gemm_pair<MODE>(map_a, map_b, map_c, args, grid, stream)
+                    : launch_gemm_single<MODE>(map_a, map_b, map_c, args, grid, stream);
+    }
 }
 
 }  // namespace lce

@@ -22,7 +22,11 @@ enum GemmMode : int {
                         //   2^P_SCALE_EXP), per-row partial sums of P, bias column sums
     MODE_GRADX = 5,     // grad_X_c = s * (P W + c W[y])         (fp16 operands, bf16 out)
     MODE_GRADW = 6,     // grad_W_acc (+)= s * P^T X_c           (fp16 operands, fp32 accumulator, bf16 cast)
+    MODE_GRADX_W = 7,   // MODE_GRADX with 256 x 512 output tiles (pair form only, N a multiple of 512): two
+                        //   N = 256 MMAs per K step fill all 512 TMEM columns, so each wave of tiles covers
+                        //   twice the rows and streams W half as often; one accumulator, not two
 };
+constexpr bool is_gradx(int mode) { return mode == MODE_GRADX || mode == MODE_GRADX_W; }
 
 // The softmax's target entry is never a tensor-core operand.  In a peaked
 // softmax (a trained head puts p ~ 0.9-0.99 on the label) a 16-bit p would
@@ -76,13 +80,24 @@ constexpr int EPI_STAGE_BYTES = EPI_WARPS * EPI_STAGE_FLOATS * 4;  // 32 KB
 // ones, whose tiles wait on the accumulator's traffic rather than the MMAs.
 constexpr int GRADW_PAIR_SLOTS = 7;
 constexpr int GRADW_PAIR_BUFS_MAX = 4;
+// MODE_GRADX_W: a K slice is A (16 KB) and two 128-column pieces of B per
+// CTA (32 KB); the ring is 4 stages deep.
+constexpr int GRADX_W_STAGES = 4;
+constexpr int pair_stage_bytes(int mode) {
+    return mode == MODE_GRADX_W ? A_STAGE_BYTES + 2 * PAIR_B_STAGE_BYTES : PAIR_STAGE_BYTES;
+}
+constexpr int pair_ring_bytes(int mode) {
+    return mode == MODE_GRADW     ? GRADW_PAIR_SLOTS * PAIR_STAGE_BYTES
+           : mode == MODE_GRADX_W ? GRADX_W_STAGES * pair_stage_bytes(mode)
+                                  : PAIR_STAGES * PAIR_STAGE_BYTES;
+}
 constexpr int gemm_smem_bytes(int mode, bool pair) {
-    return pair ? 1024 + (mode == MODE_GRADW ? GRADW_PAIR_SLOTS : PAIR_STAGES) * PAIR_STAGE_BYTES + CTL_BYTES
+    return pair ? 1024 + pair_ring_bytes(mode) + CTL_BYTES
                 : GEMM_SMEM_BYTES + (mode == MODE_GRADW ? EPI_STAGE_BYTES : 0);
 }
 static_assert(PAIR_STAGE_BYTES == EPI_STAGE_BYTES, "a ring stage and a set of epilogue buffers take the same bytes");
 static_assert(gemm_smem_bytes(MODE_GRADW, false) <= 232448 && gemm_smem_bytes(MODE_GRADW, true) <= 232448 &&
-                  gemm_smem_bytes(MODE_LSE, true) <= 232448,
+                  gemm_smem_bytes(MODE_LSE, true) <= 232448 && gemm_smem_bytes(MODE_GRADX_W, true) <= 232448,
               "shared memory of one CTA");
 
 // grad_X's last partial wave (pair form).  Each grad_X tile runs the whole
@@ -104,17 +119,20 @@ struct TailPlan {
 constexpr int TAIL_SPLIT_MAX = 8;
 constexpr int TAIL_UNITS_MAX = 320;     // tail x s partial tiles of 256 x 256 FP32 (80 MB of workspace)
 constexpr int TAIL_MIN_KBLOCKS = 16;    // shortest slice, in 64-wide k-blocks
-constexpr int64_t TAIL_TILE_FLOATS = static_cast<int64_t>(2 * BM) * BN;
+constexpr int64_t TAIL_TILE_FLOATS = static_cast<int64_t>(2 * BM) * BN;  // per 256 output columns
 
-// n_act: output tiles with valid rows; slots: pairs of the launch.
-__host__ __device__ inline TailPlan gradx_tail_plan(int n_act, int slots, int k_blocks) {
+// n_act: output tiles with valid rows; slots: pairs of the launch;
+// max_units: partial tiles the workspace holds (TAIL_UNITS_MAX, halved for
+// 512-column tiles).
+__host__ __device__ inline TailPlan gradx_tail_plan(int n_act, int slots, int k_blocks,
+                                                    int max_units = TAIL_UNITS_MAX) {
     TailPlan p{n_act > 0 ? n_act : 0, 0, 1, k_blocks};
     if (n_act <= 0 || slots <= 0) return p;
     const int r = n_act % slots;
     if (r == 0) return p;
     int best = 1, best_rounds = 1;  // tail time = best_rounds / best tiles
     for (int s = 2; s <= TAIL_SPLIT_MAX; ++s) {
-        if (r * s > TAIL_UNITS_MAX || k_blocks < s * TAIL_MIN_KBLOCKS) break;
+        if (r * s > max_units || k_blocks < s * TAIL_MIN_KBLOCKS) break;
         const int rounds = (r * s + slots - 1) / slots;
         if (rounds * best < best_rounds * s) {
             best = s;
@@ -276,7 +294,7 @@ struct GemmArgs {
 
 // Launches the GEMM kernel of `mode`: with `pair`, the pair form (grid =
 // 2 x the number of pairs; m_tiles counts 256-row tiles), else one CTA per
-// 128-row tile (grid = CTAs).  The instantiations are spread over three
+// 128-row tile (grid = CTAs).  The instantiations are spread over four
 // translation units so that they compile in parallel.
 // map_c: the grad_W accumulator's map (MODE_GRADW with acc_tma), else unused.
 cudaError_t launch_gemm(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_c,
@@ -287,6 +305,8 @@ cudaError_t launch_gemm_grads(int mode, const CUtensorMap& map_a, const CUtensor
                               const GemmArgs& args, int grid, cudaStream_t stream, bool pair);
 cudaError_t launch_gemm_plain(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_c,
                               const GemmArgs& args, int grid, cudaStream_t stream, bool pair);
+cudaError_t launch_gemm_gradx_wide(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_c,
+                                   const GemmArgs& args, int grid, cudaStream_t stream, bool pair);
 // Pairs of the pair form that can be resident at once on this device (0 if
 // the form cannot launch).
 int gemm_pair_slots();
@@ -339,8 +359,9 @@ cudaError_t launch_gradx_split_reduce(const float* split_out, int64_t splits, in
                                       int64_t ignore_index, int64_t V, const uint16_t* W, const float* tcoef,
                                       const WsHeader* hdr, uint16_t* grad_X_chunk, cudaStream_t s);
 // Finishes the split tail tiles of one grad_X launch of the pair form (slots:
-// its pairs; n_tiles, k_blocks: its tile columns and K extent).
-cudaError_t launch_gradx_tail_reduce(const float* tail_out, int slots, int n_tiles, int k_blocks, int64_t H,
+// its pairs; n_tiles, k_blocks: its tile columns and K extent; nw: 1 for
+// 256-column tiles, 2 for 512).
+cudaError_t launch_gradx_tail_reduce(const float* tail_out, int slots, int n_tiles, int k_blocks, int nw, int64_t H,
                                      const int* crow, const int* n_valid, int64_t max_rows, const int64_t* y,
                                      int64_t ignore_index, int64_t V, const uint16_t* W, const float* tcoef,
                                      const WsHeader* hdr, uint16_t* grad_X_chunk, cudaStream_t s);

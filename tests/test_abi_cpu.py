@@ -231,9 +231,18 @@ def test_gradx_tail_plan(tiles, slots, kb, want):
     assert lce.lce_debug_gradx_tail_plan(tiles, slots, kb) == want
 
 
+@pytest.mark.parametrize("tiles,slots,kb,want", [
+    (248, 76, 2374, (228, 20, 7, 340)),   # 256 x 512 tiles of an 8192-row chunk (7782 valid rows), H = 4096
+    (64, 76, 64, (64, 0, 1, 64)),         # 64 x 4 slices would pass the 160 partial tiles of 512 columns
+    (20, 76, 128, (0, 20, 7, 19)),
+])
+def test_gradx_tail_plan_wide_tiles(tiles, slots, kb, want):
+    assert lce.lce_debug_gradx_tail_plan(tiles, slots, kb, 512) == want
+
+
 def test_gradx_tail_plan_properties():
     """On random launches: the slices cover K without an empty one, the
-    partial tiles fit the workspace's 320, and the split taken is the
+    partial tiles fit the workspace (320 of 256 columns, 160 of 512), and the split taken is the
     shortest tail among the allowed ones (none when none saves an eighth)."""
     rng = __import__("random").Random(5)
 
@@ -244,22 +253,24 @@ def test_gradx_tail_plan_properties():
         slots = rng.choice([1, 2, 37, 75, 76, 80, 148])
         tiles = rng.randrange(0, 6 * slots + 3)
         kb = rng.choice([1, 15, 32, 64, 127, 128, 2374, rng.randrange(1, 3000)])
-        full, tail, s, kps = lce.lce_debug_gradx_tail_plan(tiles, slots, kb)
+        cols = rng.choice([256, 512])
+        full, tail, s, kps = lce.lce_debug_gradx_tail_plan(tiles, slots, kb, cols)
+        cap = 320 * 256 // cols
         r = tiles % slots
-        allowed = [t for t in range(2, 9) if r * t <= 320 and kb >= 16 * t]
+        allowed = [t for t in range(2, 9) if r * t <= cap and kb >= 16 * t]
         good = [t for t in allowed if 8 * -(-r * t // slots) <= 7 * t]
         if tail == 0:
             assert (full, s, kps) == (tiles, 1, kb)
             assert r == 0 or not good
             continue
         assert full + tail == tiles and full % slots == 0 and tail == r
-        assert 2 <= s <= 8 and tail * s <= 320 and (s - 1) * kps < kb <= s * kps and kps >= 16
+        assert 2 <= s <= 8 and tail * s <= cap and (s - 1) * kps < kb <= s * kps and kps >= 16
         assert 8 * -(-tail * s // slots) <= 7 * s
         assert all(tail_time(r, s, slots) <= tail_time(r, t, slots) for t in allowed)
 
 
 def test_gradx_tail_plan_rejects():
-    for args in [(-1, 76, 10), (10, -1, 10), (10, 76, -1), (2**31, 76, 10)]:
+    for args in [(-1, 76, 10), (10, -1, 10), (10, 76, -1), (2**31, 76, 10), (10, 76, 10, 384)]:
         with pytest.raises(lce.LCEError) as e:
             lce.lce_debug_gradx_tail_plan(*args)
         assert e.value.status == 1

@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 FILES = ["tests/test_gpu_parity.py", "tests/test_gpu_peaked.py", "tests/test_gpu_options.py",
-         "tests/test_gpu_random_shapes.py", "tests/test_gpu_extremes.py"]
+         "tests/test_gpu_random_shapes.py", "tests/test_gpu_extremes.py", "tests/test_gpu_gradx_tail.py"]
 
 
 def test_child_process_loads_the_debug_library():

@@ -1,14 +1,15 @@
 """grad_X of the pair form with its last partial round of tiles split over
 the vocabulary (K), against the FP64 oracle.
 
-Each grad_X tile of 256 rows x 256 columns runs the whole vocabulary as its
-K loop, so a launch whose tile count leaves the last round of pairs partly
-idle splits the tiles of that round into K slices and adds their partial
-sums in slice order.  The valid-row counts of these cases are fixed (exact
-ignore counts), so the split each chunk takes is known from the plan
-function the kernels use (lce_debug_gradx_tail_plan); the cases cover a
-split after whole rounds, a chunk that is all tail, and a ragged last chunk
-of the overlapped schedule."""
+Each grad_X tile of 256 rows x 256 columns (x 512 where H is a multiple of
+512) runs the whole vocabulary as its K loop, so a launch whose tile count
+leaves the last round of pairs partly idle splits the tiles of that round
+into K slices and adds their partial sums in slice order.  The valid-row
+counts of these cases are fixed (exact ignore counts), so the split each
+chunk takes is known from the plan function the kernels use
+(lce_debug_gradx_tail_plan); the cases cover, for both tile widths, a split
+after whole rounds and a chunk that is all tail, and a ragged last chunk of
+the overlapped schedule."""
 import numpy as np
 import pytest
 
@@ -28,9 +29,10 @@ def plans(N, H, V, chunk, y):
     for r0 in range(0, N, C):
         rows = min(C, N - r0)
         valid = int((y[r0:r0 + rows] != L.IGNORE_INDEX).sum())
-        tiles = -(-valid // 256) * -(-H // 256)
-        grid = min(slots, -(-rows // 256) * -(-H // 256) * 8)
-        out.append(lce.lce_debug_gradx_tail_plan(tiles, grid, -(-V // 64)))
+        cols = 512 if H % 512 == 0 else 256  # the library's tile width
+        tiles = -(-valid // 256) * -(-H // cols)
+        grid = min(slots, -(-rows // 256) * -(-H // cols) * 8)
+        out.append(lce.lce_debug_gradx_tail_plan(tiles, grid, -(-V // 64), cols))
     return out
 
 
@@ -44,11 +46,15 @@ def problem(seed, N, H, V, ignored):
 
 # (N, H, V, chunk rows, ignored rows, the plans on a 76-pair device: (whole tiles, split tiles, slices, k-blocks))
 CASES = [
-    # one chunk, 2048 valid rows: 128 tiles, one whole round of 76, 52 tiles in 4 slices
-    (2560, 4096, 4096, 0, 512, [(76, 52, 4, 16)]),
-    # one chunk, 1280 valid rows: 40 tiles, all split (7 slices of 19 k-blocks; the last of 14)
-    (2560, 2048, 8192, 0, 1280, [(0, 40, 7, 19)]),
-    # 4096-row chunks (overlapped schedule) and a ragged last chunk of 1000 rows
+    # 512-column tiles; 5530 valid rows: 22 x 4 = 88 tiles, one whole round of 76, 12 tiles in 4 slices
+    (6144, 2048, 4096, 0, 614, [(76, 12, 4, 16)]),
+    # 512-column tiles; 1280 valid rows: 20 tiles, all split (7 slices of 19 k-blocks; the last of 14)
+    (2560, 2048, 8192, 0, 1280, [(0, 20, 7, 19)]),
+    # 256-column tiles (H = 2304); 2868 valid rows: 12 x 9 = 108 tiles, 76 whole, 32 in 2 slices
+    (4096, 2304, 4096, 0, 1228, [(76, 32, 2, 32)]),
+    # 256-column tiles; 1280 valid rows: 45 tiles, all split in 3 slices
+    (2560, 2304, 4096, 0, 1280, [(0, 45, 3, 22)]),
+    # 4096-row chunks (overlapped schedule), 512-column tiles, and a ragged last chunk of 1000 rows
     (9192, 2048, 4096, 4096, 919, None),
 ]
 
