@@ -298,11 +298,15 @@ LCE_API lce_status_t lce_static_ws_check_status(lce_stream_t stream);
  *   LCE_GEMM_PAIR: a cluster of two CTAs on neighbouring SMs computes
  *     256x256 tiles with one tcgen05.mma of M = 256 (cta_group::2); each
  *     SM loads its own half of B, so a 64-wide K slice brings 32 KB into
- *     each SM instead of 48 KB, and the ring is 6 stages deep.  On a device
+ *     each SM instead of 48 KB, and the ring is 6 stages deep.  grad_X
+ *     uses 256x512 tiles where H is a multiple of 512, and splits the tiles
+ *     of its last, partly filled round over the vocabulary.  On a device
  *     that cannot keep any cluster of two resident, calls use SINGLE.
  * The products are the ones the documentation of each entry point states
  * in either form.  The forms may differ in the last bits of FP32 sums;
- * each form is deterministic.  The workspace does not depend on the form.
+ * each form is deterministic on a given device (grad_X's split depends on
+ * the device's number of pairs).  The workspace does not depend on the
+ * form.
  * Returns the previous form, or -1 for an unknown value (nothing changes).
  * Host-only; safe to call from any thread. */
 #define LCE_GEMM_SINGLE 0
