@@ -828,7 +828,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (gradw_reads_old(args) && c0 < args.N)
                     gradw_load_old(args, static_cast<int64_t>(m) * BM + q * 32, m_rows, c0, lane, pre);
             }
-            if (!wait_phase(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, args.status, limit)) break;
+            // (a warp vote keeps the lanes together should their waits end differently)
+            if (!__all_sync(0xFFFFFFFFu, wait_phase(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, args.status, limit)))
+                break;
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             epilogue_tile<MODE>(args, m, n, q, half, lane, taddr, smem_u32(&ctl->tmem_empty[acc]), m_rows,

@@ -4,6 +4,9 @@
 // and its own half of B (128 of the tile's 256 columns), so a 64-element K
 // slice costs each SM 32 KB of shared memory and L2 traffic instead of the
 // single-CTA form's 48 KB, and the ring is 6 stages deep instead of 4.
+// grad_X with 256 x 512 tiles (MODE_GRADX_W) issues two such MMAs per K step
+// into one 512-column accumulator, from 48 KB slices in a 4-stage ring;
+// grad_W shares 7 slots of 32 KB between its ring and its epilogue buffers.
 //
 //   warp 0 (one lane, both CTAs): TMA producer of the CTA's own halves.
 //          Both CTAs' copies of a slice complete on rank 0's `full` barrier
@@ -64,8 +67,8 @@ __device__ __forceinline__ bool wait_phase_pair(uint32_t bar, uint32_t parity, S
 // TMA load that many blocks ahead, the lanes add s times the accumulator in
 // place, and a TMA store writes the block back.  Block g of a warp is
 // 32-column slab g & 3 of its half of the tile of unit cid + (g >> 2) ncl.
-// (The plain loads and stores keep the DRAM stream full where the L2-side
-// adds of acc_tma 1 leave it idle part of the time.)
+// (Measured on short K loops: the plain loads and stores move the
+// accumulator faster than the L2-side adds of acc_tma 1.)
 struct OldBlocks {
     float* buf;      // the warp's first buffer
     uint32_t sbuf;   // its shared-memory address
@@ -119,7 +122,9 @@ static __device__ __noinline__ bool gradw_tile_old(const GemmArgs& a, const OldB
         float v[32];
         tmem_load_32cols(taddr + 32 * (j0 + jj), v);
         const uint32_t b = g & (L.nbuf - 1);
-        if (!wait_phase_pair(L.bars + 8u * b, (g >> L.lg) & 1u, ctl, peer_abort, a.status, limit)) {
+        // (a warp vote keeps the lanes together should their waits end differently)
+        if (!__all_sync(0xFFFFFFFFu, wait_phase_pair(L.bars + 8u * b, (g >> L.lg) & 1u, ctl, peer_abort, a.status,
+                                                     limit))) {
             ok = false;
             break;
         }
@@ -408,7 +413,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 if (gradw_reads_old(args) && c0 < args.N)
                     gradw_load_old(args, static_cast<int64_t>(mc) * BM + q * 32, m_rows, c0, lane, pre);
             }
-            if (!wait_phase_pair(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, peer_abort, args.status, limit)) {
+            // (a warp vote keeps the lanes together should their waits end differently)
+            if (!__all_sync(0xFFFFFFFFu, wait_phase_pair(smem_u32(&ctl->tmem_full[acc]), acc_phase, ctl, peer_abort,
+                                                         args.status, limit))) {
                 old_ok = false;
                 break;
             }
