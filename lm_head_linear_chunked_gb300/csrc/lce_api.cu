@@ -37,6 +37,8 @@ constexpr int64_t GROUP_BYTES = 32ll << 20;
 // over K (the vocabulary) so that about two waves of tiles fill the GPU;
 // the target does not depend on the device, so neither does the workspace.
 constexpr int64_t GRADX_TARGET_TILES = 304;
+// Shortest K slice of a split grad_X product that takes 512-column tiles.
+constexpr int64_t GRADX_W_MIN_SPLIT_KBLOCKS = 48;
 
 int64_t gradx_splits(int64_t C, int64_t H, int64_t V) {
     const int64_t tiles = cdiv(C, BM) * cdiv(H, BN);
@@ -487,13 +489,18 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             !map_16bit_2d(&mX16_mn, X16, rows, pb.H, pb.H, 64, 64, true))
             return LCE_ERR_CUDA;
         if (o.grad_X) {   // grad_X_c = s (P W - W[y])
-            // pair form with the tail split and H a multiple of 512: 256 x 512 tiles
-            const bool wide = tail != nullptr && pb.H % (2 * BN) == 0;
+            // pair form and H a multiple of 512: 256 x 512 tiles, whole (with the tail
+            // split) or as the K slices of a small chunk's split product when those
+            // are long enough to hide the wide tile's unoverlapped partial store
+            // (measured: 63-block slices 3% faster, 14-block slices 5% slower)
+            const int64_t kbl = cdiv(pb.V, BK);
+            const bool wide = form.pair && pb.H % (2 * BN) == 0 &&
+                              (p.gradx_splits <= 1 || cdiv(kbl, p.gradx_splits) >= GRADX_W_MIN_SPLIT_KBLOCKS);
             const int nw = wide ? 2 : 1;
             GemmArgs a = call_args();
             a.m_tiles = static_cast<int32_t>(mtf);
             a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN * nw));
-            a.k_blocks = static_cast<int32_t>(cdiv(pb.V, BK));
+            a.k_blocks = static_cast<int32_t>(kbl);
             // pair form: H tiles fastest, so that each wave covers whole rows of
             // grad_X and every tile sharing a P row block runs at once (measured:
             // grad_X 7% faster and ~20% fewer DRAM reads than 2048-row groups)
