@@ -56,6 +56,8 @@ CASES = [
     (2560, 2304, 4096, 0, 1280, [(0, 45, 3, 22)]),
     # 4096-row chunks (overlapped schedule), 512-column tiles, and a ragged last chunk of 1000 rows
     (9192, 2048, 4096, 4096, 919, None),
+    # one column of 512-wide tiles (H = 512) in one 10240-row chunk: 36 tiles, all split in 2 slices
+    (10240, 512, 4096, 10240, 1024, [(0, 36, 2, 32)]),
 ]
 
 
