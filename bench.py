@@ -75,6 +75,34 @@ def gemm_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
+def role_bytes(H: int, V: int, rows, valid, overlapped: bool) -> dict:
+    """Algorithmic DRAM bytes per step of each GEMM role of the fused call:
+    each operand read once, each result written once, per chunk.  rows[c] and
+    valid[c]: chunk c's rows and valid rows (the backward runs on valid rows
+    only).
+      logits_lse: X_c, W, E of the valid rows written; with the overlapped
+        schedule also the previous chunk's E read and P written (its side job;
+        the last chunk's rescale is a separate kernel).
+      grad_x: P and W16 read, grad_X rows written (nothing for a chunk without
+        valid rows).
+      grad_w: P and X16 read; the FP32 accumulator written (first chunk), read
+        and written (later chunks), plus its bf16 cast written (last chunk); a
+        chunk between the first and the last without valid rows adds nothing."""
+    n = len(rows)
+    fwd = sum(2 * r * H + 2 * V * H + 2 * v * V for r, v in zip(rows, valid))
+    if overlapped:
+        fwd += sum(4 * v * V for v in valid[:-1])
+    gx = sum(2 * v * V + 2 * V * H + 2 * v * H for v in valid if v > 0)
+    gw = 0
+    for c, v in enumerate(valid):
+        first, last = c == 0, c == n - 1
+        if v == 0 and not first and not last:
+            continue
+        acc = (4 if first else 8) * V * H + (2 * V * H if last else 0)
+        gw += 2 * v * V + 2 * v * H + acc
+    return {"logits_lse": float(fwd), "grad_x": float(gx), "grad_w": float(gw)}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -521,7 +549,19 @@ def run_ours(args, w):
     dom_tflops = dom_flops_per_launch / (dom_ms / role_chunks / 1e3) / 1e12
     sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     total_launches = sum(v[1] for v in prof.values())
+    # Which peak bounds each role: the time its FLOPs take at the sustained
+    # tensor peak against the time its algorithmic bytes take at the measured
+    # copy bandwidth (small chunks make grad_W, for one, bandwidth-bound).
+    chunk_rows = [min(C, N - r0) for r0 in range(0, N, C)]
+    yv = (yh != -100)
+    chunk_valid = [int(yv[r0:r0 + C].sum().item()) for r0 in range(0, N, C)]
+    rbytes = role_bytes(H, V, chunk_rows, chunk_valid, overlapped)
+    role_bound = {k: ("hbm" if rbytes[k] / (hbm * 1e9) > 2.0 * N * H * V / (sustained * 1e12) else "tensor")
+                  for k in rbytes}
+    dom_bound = role_bound.get(dom, "tensor")
+    dom_gbs = rbytes.get(dom, 0.0) / (dom_ms / args.steps / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": replica_rate(N, ws_n, t_step), "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * t_step, "higher_is_better": True, "scaling": "weak",
@@ -586,6 +626,27 @@ def run_ours(args, w):
         "e2e": e2e,
         "separate_entry_points": split,
     }
+    for k, r in line["roofline"]["roles"].items():  # each role's bound and its bandwidth figure
+        if k in rbytes:
+            r["bound"] = role_bound[k]
+            r["gbs"] = rbytes[k] / (prof[k][0] / args.steps / 1e3) / 1e9
+            r["frac_hbm"] = r["gbs"] / hbm
+    if dom_bound == "hbm":
+        # the dominant role is bandwidth-bound (e.g. grad_W at small chunks): the
+        # roofline is its algorithmic bytes against the measured copy rate, and the
+        # tensor figures stay beside it
+        tensor_view = line["roofline"]
+        line["roofline"] = {
+            "bound": "hbm", "achieved": dom_gbs, "peak": hbm, "unit": "GB/s", "frac": dom_gbs / hbm,
+            "peak_kind": f"{peak_src} HBM copy rate",
+            "algorithmic_bytes": rbytes[dom] / n_chunks,
+            "algorithmic_bytes_note": "per launch: the mean over the step's chunks of the operands read once, the "
+                                      "results written once, and the FP32 grad_W accumulator read and written per "
+                                      "chunk",
+            "traffic": None, "traffic_source": "no ncu capture for this workload's launches",
+            "kernel": tensor_view["kernel"], "roles": tensor_view.pop("roles"),
+            "tensor_view": tensor_view,
+        }
     if not args.no_cpu_baseline and ws_n == 1:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_rows)
     print(json.dumps(line), flush=True)
