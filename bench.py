@@ -420,7 +420,8 @@ def run_ours(args, w):
                              ws_b, nws_b, s)
 
         split = {}
-        for name, fn, fl in (("forward", fwd, 2.0 * N * H * V), ("backward", bwd, 6.0 * N * H * V)):
+        nv_rows = int((yh != -100).sum().item())  # the gradient products run over the valid rows only
+        for name, fn, fl in (("forward", fwd, 2.0 * N * H * V), ("backward", bwd, 2.0 * (N + 2 * nv_rows) * H * V)):
             for _ in range(2):
                 fn()
             a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -533,19 +534,22 @@ def run_ours(args, w):
     tflops = flops / t_step / 1e12
     C = lce.lce_chunk_rows(N, H, V, chunk)
     n_chunks = -(-N // C)
-    # dominant kernel: the GEMM role with the most device time; each launch
-    # does 2 * rows * H * V FLOPs
+    # dominant kernel: the GEMM role with the most device time
     gemm_kinds = ["logits_lse", "recomputed_logits_softmax", "grad_x", "grad_w"]
     dom = max(gemm_kinds, key=lambda k: prof[k][0])
     # the fused call's schedule: the forward rescales the previous chunk (no p_rescale launches but the last)
     overlapped = nws > lce.lce_workspace_size(N, H, V, chunk, has_b, lce.WS_FUSED_MIN)
-    # tensor-core FLOPs the step executes: 2NHV per GEMM role that ran
-    executed = sum(2.0 * N * H * V for k in gemm_kinds if prof[k][1] > 0)
+    # FLOPs each role executes per step: the logits passes run over all N rows
+    # (lse is written for every row), the gradient products over the valid rows
+    # only (ignored rows are compacted away)
+    n_valid_rows = int((yh != -100).sum().item())
+    role_flops = {k: 2.0 * (n_valid_rows if k in ("grad_x", "grad_w") else N) * H * V for k in gemm_kinds}
+    executed = sum(role_flops[k] for k in gemm_kinds if prof[k][1] > 0)
     dom_ms, dom_n = prof[dom]
     # each GEMM role runs once per chunk; a split grad_X product adds its
     # reduction kernel to the role, so time is counted per chunk, not per launch
     role_chunks = args.steps * n_chunks
-    dom_flops_per_launch = 2.0 * N * H * V / n_chunks
+    dom_flops_per_launch = role_flops[dom] / n_chunks
     dom_tflops = dom_flops_per_launch / (dom_ms / role_chunks / 1e3) / 1e12
     sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
@@ -558,7 +562,7 @@ def run_ours(args, w):
     yv = (yh != -100)
     chunk_valid = [int(yv[r0:r0 + C].sum().item()) for r0 in range(0, N, C)]
     rbytes = role_bytes(H, V, chunk_rows, chunk_valid, overlapped)
-    role_bound = {k: ("hbm" if rbytes[k] / (hbm * 1e9) > 2.0 * N * H * V / (sustained * 1e12) else "tensor")
+    role_bound = {k: ("hbm" if rbytes[k] / (hbm * 1e9) > role_flops[k] / (sustained * 1e12) else "tensor")
                   for k in rbytes}
     dom_bound = role_bound.get(dom, "tensor")
     dom_gbs = rbytes.get(dom, 0.0) / (dom_ms / args.steps / 1e3) / 1e9
@@ -583,8 +587,9 @@ def run_ours(args, w):
                                   "measured_sustained_bf16": executed / t_step / 1e12 / sustained,
                                   "nominal_dense_bf16_2250": executed / t_step / 1e12 / 2250.0,
                                   "peak_source": peak_src,
-                                  "flops": "tensor-core FLOPs the step executes: 2*N*H*V per GEMM role that ran "
-                                           "(forward logits, grad_X, grad_W = 6*N*H*V in the fused call)"},
+                                  "flops": "tensor-core FLOPs the step executes: 2*N*H*V for the logits pass and "
+                                           "2*n_valid*H*V for each gradient product, which run over the valid rows "
+                                           "only (2*N*H*V + 4*n_valid*H*V in the fused call)"},
         "workspace_note": "the fused call keeps each chunk's fp16 exponentials in the workspace instead of "
                           "recomputing the logits tile in the backward",
         "roofline": {"bound": "tensor", "achieved": dom_tflops, "peak": sustained, "unit": "TFLOP/s",
@@ -601,8 +606,8 @@ def run_ours(args, w):
                      "kernel": f"{'gemm_pair_kernel' if gemm_form == 'pair' else 'gemm_kernel'} ({dom})" + (
                          ", which also turns the previous chunk's kept exponentials into the softmax (4*C*V bytes) "
                          "with its epilogue warps" if dom == "logits_lse" and overlapped else ""),
-                     "roles": {k: {"tflops": 2.0 * N * H * V / n_chunks / (prof[k][0] / role_chunks / 1e3) / 1e12,
-                                   "frac": 2.0 * N * H * V / n_chunks / (prof[k][0] / role_chunks / 1e3) / 1e12 /
+                     "roles": {k: {"tflops": role_flops[k] / n_chunks / (prof[k][0] / role_chunks / 1e3) / 1e12,
+                                   "frac": role_flops[k] / n_chunks / (prof[k][0] / role_chunks / 1e3) / 1e12 /
                                    sustained, "ms_per_chunk": prof[k][0] / role_chunks,
                                    "launches_per_chunk": prof[k][1] / role_chunks}
                                for k in gemm_kinds if prof[k][1] > 0},
