@@ -37,8 +37,6 @@ constexpr int64_t GROUP_BYTES = 32ll << 20;
 // over K (the vocabulary) so that about two waves of tiles fill the GPU;
 // the target does not depend on the device, so neither does the workspace.
 constexpr int64_t GRADX_TARGET_TILES = 304;
-// Shortest K slice of a split grad_X product that takes 512-column tiles.
-constexpr int64_t GRADX_W_MIN_SPLIT_KBLOCKS = 48;
 
 int64_t gradx_splits(int64_t C, int64_t H, int64_t V) {
     const int64_t tiles = cdiv(C, BM) * cdiv(H, BN);
@@ -489,14 +487,19 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             !map_16bit_2d(&mX16_mn, X16, rows, pb.H, pb.H, 64, 64, true))
             return LCE_ERR_CUDA;
         if (o.grad_X) {   // grad_X_c = s (P W - W[y])
-            // pair form and H a multiple of 512: 256 x 512 tiles, whole (with the tail
-            // split) or as the K slices of a small chunk's split product when those
-            // are long enough to hide the wide tile's unoverlapped partial store
-            // (measured: 63-block slices 3% faster, 14-block slices 5% slower)
+            // pair form and H a multiple of 512: 256 x 512 tiles (with the tail split)
             const int64_t kbl = cdiv(pb.V, BK);
-            const bool wide = form.pair && pb.H % (2 * BN) == 0 &&
-                              (p.gradx_splits <= 1 || cdiv(kbl, p.gradx_splits) >= GRADX_W_MIN_SPLIT_KBLOCKS);
+            const bool wide = form.pair && pb.H % (2 * BN) == 0 && p.gradx_splits <= 1;
             const int nw = wide ? 2 : 1;
+            // A small chunk's split product in the pair form: K slices for one round
+            // of the pairs, fewer than the workspace holds (measured against two
+            // rounds, or 512-column tiles: half the FP32 partial sums to write and
+            // add, grad_X 10-14% faster at 256-row chunks)
+            int64_t splits = p.gradx_splits;
+            if (form.pair && splits > 1) {
+                const int64_t sp = cdiv(static_cast<int64_t>(form.slots), mtf * cdiv(pb.H, BN));
+                if (sp < splits) splits = sp > 1 ? cdiv(kbl, cdiv(kbl, sp)) : 1;
+            }
             GemmArgs a = call_args();
             a.m_tiles = static_cast<int32_t>(mtf);
             a.n_tiles = static_cast<int32_t>(cdiv(pb.H, BN * nw));
@@ -520,8 +523,8 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             a.row_map = crow + r0;
             a.tcoef = tcoef + r0;
             a.dyn_rows = nvc + c;
-            a.k_splits = static_cast<int32_t>(p.gradx_splits);
-            a.k_per_split = static_cast<int32_t>(cdiv(a.k_blocks, p.gradx_splits));
+            a.k_splits = static_cast<int32_t>(splits);
+            a.k_per_split = static_cast<int32_t>(cdiv(a.k_blocks, splits));
             a.split_out = split_out;
             a.split_stride = p.C * pb.H;
             a.tail_out = tail;
@@ -529,15 +532,15 @@ lce_status_t run(const Problem& pb, const Outputs& o, bool do_fwd, bool do_bwd, 
             // with the tail split, a chunk of fewer tiles than pairs still gets every
             // pair: its slices spread over them
             const int grid = grid_of(form, static_cast<int64_t>(a.m_tiles) * a.n_tiles *
-                                               (tail ? TAIL_SPLIT_MAX : p.gradx_splits));
+                                               (tail ? TAIL_SPLIT_MAX : splits));
             LCE_LAUNCH(PK_GRADX, launch_gemm(wide ? MODE_GRADX_W : MODE_GRADX, mG_k, mW16_mn, mW16_mn, a, grid, s,
                                              form.pair));
             if (tail)  // the same plan as the GEMM's: its pairs, tile columns and K extent
                 LCE_LAUNCH(PK_GRADX, launch_gradx_tail_reduce(tail, grid / 2, a.n_tiles, a.k_blocks, nw, pb.H, crow + r0,
                                                               nvc + c, rows, pb.y + r0, pb.ignore_index, pb.V, pb.W,
                                                               tcoef + r0, hdr, o.grad_X + r0 * pb.H, s));
-            if (split_out)
-                LCE_LAUNCH(PK_GRADX, launch_gradx_split_reduce(split_out, p.gradx_splits, p.C * pb.H, pb.H, crow + r0,
+            if (split_out && splits > 1)
+                LCE_LAUNCH(PK_GRADX, launch_gradx_split_reduce(split_out, splits, p.C * pb.H, pb.H, crow + r0,
                                                                nvc + c, rows, pb.y + r0, pb.ignore_index, pb.V,
                                                                pb.W, tcoef + r0, hdr, o.grad_X + r0 * pb.H, s));
         }
